@@ -1,0 +1,166 @@
+"""Seeded synthetic inputs for verify attention.
+
+This module only draws numbers and lays down the workload recipes (shapes, seeds,
+positions, value distributions).  It holds none of the attention arithmetic, so the
+CUDA path and the CPU oracle can both be fed from it without sharing any method code.
+
+Recipes (IQuestRT technical report: 8 verify rows x 6 query heads per KV head,
+head_dim 128, 1K-192K context sweep with synthetic KV, sliding window 4,096 in a
+4,160-slot ring):
+
+  tiny      capacity 1,024, rows at positions 1016..1023, 5 live rows, 4 splits
+  16k       capacity 65,536, 16,384 valid positions, 8 live rows, 5 % of keys x4
+  swa       window 4,096, ring 4,160, context 40,000 (ring wrapped), 7 live rows
+  192k      196,608 positions (about 100 MB of K/V), n_live 4..8
+  sweep     {1K,4K,16K,32K,64K,128K,192K} x {full, swa} x n_live 4..8
+
+Q, K, V ~ N(0, 1) drawn in float32 by a seeded CPU torch generator and rounded to
+bf16; sink ~ N(0, 1) float32; scale = 1/sqrt(128).
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+HEAD_DIM = 128
+Q_HEADS = 6
+N_ROWS = 8
+SCALE = 1.0 / math.sqrt(128.0)
+WINDOW = 4096
+RING_SLOTS = 4160
+SWEEP_CONTEXTS = (1024, 4096, 16384, 32768, 65536, 131072, 196608)
+
+# bf16 bit patterns used to poison cache slots the kernels must not use
+BF16_NAN = 0x7FC0
+BF16_K_SENTINEL = 0x4280   # 64.0
+BF16_V_SENTINEL = 0x447A   # 1000.0
+
+
+@dataclasses.dataclass
+class Workload:
+    """One verify call.  Tensors are CPU tensors; bf16 data is stored as torch.bfloat16."""
+    name: str
+    seed: int
+    q: torch.Tensor            # [n_rows, 6, 128] bf16
+    k_hist: torch.Tensor       # [ctx, 128] bf16, row j = absolute position j
+    v_hist: torch.Tensor       # [ctx, 128] bf16
+    pos: torch.Tensor          # [n_rows] int32, 0-based absolute positions
+    n_live: int
+    sink: torch.Tensor         # [6] float32
+    scale: float
+    window: int                # 0 = full attention
+    slots: int                 # full: cache capacity; swa: ring slots
+    n_splits: int              # 0 = auto
+    poison_tail: bool = True   # full cache: slots at and beyond the valid extent hold NaN
+
+    @property
+    def n_rows(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def ctx(self) -> int:
+        return int(self.k_hist.shape[0])
+
+
+def generator(seed: int) -> torch.Generator:
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    return g
+
+
+def normal_bf16(shape, g: torch.Generator, scale: float = 1.0) -> torch.Tensor:
+    x = torch.randn(*shape, generator=g, dtype=torch.float32)
+    if scale != 1.0:
+        x = x * scale
+    return x.to(torch.bfloat16)
+
+
+def tail_positions(ctx: int, n_live: int, n_rows: int = N_ROWS) -> torch.Tensor:
+    """Rows at the end of the context: pos[r] = ctx - n_live + r (padding rows continue past it)."""
+    return torch.tensor([ctx - n_live + r for r in range(n_rows)], dtype=torch.int32)
+
+
+def make(name: str, seed: int, ctx: int, n_live: int, window: int = 0, slots: int = 0,
+         n_splits: int = 0, peaky_frac: float = 0.0, pos: torch.Tensor | None = None,
+         n_rows: int = N_ROWS, poison_tail: bool = True) -> Workload:
+    """Draw one workload.  `ctx` positions of history are generated (the live rows' own K/V
+    included, at their positions)."""
+    g = generator(seed)
+    q = normal_bf16((n_rows, Q_HEADS, HEAD_DIM), g)
+    k = torch.randn(ctx, HEAD_DIM, generator=g, dtype=torch.float32)
+    if peaky_frac > 0.0:
+        n_peaky = int(round(peaky_frac * ctx))
+        idx = torch.randperm(ctx, generator=g)[:n_peaky]
+        k[idx] *= 4.0
+    k = k.to(torch.bfloat16)
+    v = normal_bf16((ctx, HEAD_DIM), g)
+    sink = torch.randn(Q_HEADS, generator=g, dtype=torch.float32)
+    if pos is None:
+        pos = tail_positions(ctx, n_live, n_rows)
+    if slots <= 0:
+        slots = RING_SLOTS if window > 0 else ctx
+    return Workload(name=name, seed=seed, q=q, k_hist=k, v_hist=v, pos=pos.to(torch.int32), n_live=n_live,
+                    sink=sink, scale=SCALE, window=window, slots=slots, n_splits=n_splits,
+                    poison_tail=poison_tail)
+
+
+def tiny(poison_tail: bool = False) -> Workload:
+    """Context 1,024, rows at 1-based positions 1017..1024 (0-based 1016..1023), 5 live, 4 splits."""
+    pos = torch.arange(1016, 1024, dtype=torch.int32)
+    return make("tiny", 1, ctx=1024, n_live=5, slots=1024, n_splits=4, pos=pos, poison_tail=poison_tail)
+
+
+def full_16k() -> Workload:
+    """Capacity 65,536, 16,384 valid positions, 8 live rows at the tail, 5 % of keys x4."""
+    w = make("16k", 2, ctx=16384, n_live=8, slots=65536, n_splits=0, peaky_frac=0.05)
+    return w
+
+
+def swa_40k() -> Workload:
+    """Window 4,096 in a 4,160-slot ring at absolute context 40,000; 7 live rows at 39,993..39,999."""
+    pos = torch.tensor([39993 + r for r in range(N_ROWS)], dtype=torch.int32)
+    return make("swa", 3, ctx=40000, n_live=7, window=WINDOW, slots=RING_SLOTS, n_splits=0, pos=pos)
+
+
+def full_192k(n_live: int) -> Workload:
+    """196,608 positions, capacity 196,672 (NaN tail), rows at the tail."""
+    return make(f"192k_n{n_live}", 4 + n_live, ctx=196608, n_live=n_live, slots=196672, n_splits=0)
+
+
+def sweep_points():
+    """(index, ctx, window, n_live) of the 70 sweep points."""
+    pts = []
+    idx = 0
+    for ctx in SWEEP_CONTEXTS:
+        for window in (0, WINDOW):
+            for n_live in (4, 5, 6, 7, 8):
+                pts.append((idx, ctx, window, n_live))
+                idx += 1
+    return pts
+
+
+def sweep(idx: int, ctx: int, window: int, n_live: int) -> Workload:
+    slots = RING_SLOTS if window > 0 else ctx + 64
+    kind = "swa" if window > 0 else "full"
+    return make(f"sweep_{kind}_{ctx}_n{n_live}", 100 + idx, ctx=ctx, n_live=n_live, window=window,
+                slots=slots, n_splits=0)
+
+
+def random_partials(seed: int, n_splits: int, n_rows: int, n_live: int, empty_frac: float = 0.1):
+    """Synthetic split partials for testing the merge on its own: o ~ N(0,1) fp32,
+    lse ~ N(0, 3) fp32 with a fraction set to -inf (empty splits), sink ~ N(0, 1)."""
+    g = generator(seed)
+    part_o = torch.randn(n_splits, n_rows, Q_HEADS, HEAD_DIM, generator=g, dtype=torch.float32)
+    part_lse = torch.randn(n_splits, n_rows, Q_HEADS, generator=g, dtype=torch.float32) * 3.0
+    empty = torch.rand(n_splits, n_rows, Q_HEADS, generator=g) < empty_frac
+    part_lse[empty] = float("-inf")
+    part_o[empty] = 0.0
+    sink = torch.randn(Q_HEADS, generator=g, dtype=torch.float32)
+    return part_o, part_lse, sink
+
+
+def bits(t: torch.Tensor) -> torch.Tensor:
+    """bf16 tensor -> its int16 bit patterns (same storage size)."""
+    return t.contiguous().view(torch.int16)

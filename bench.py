@@ -1,0 +1,393 @@
+#!/usr/bin/env python3
+"""Throughput of the verify-attention step on GB300.
+
+Workload (one step): a full-attention layer at 196,608 positions (about 100.7 MB of bf16 K/V),
+one KV head serving six query heads, head_dim 128, eight verify rows with n_live swept 4..8 - one
+call per n_live, each call = kv_ring_append + verify_attn_full (split-KV over every SM) +
+attn_split_combine.  Each n_live has its own cache (seeds 8..12), so five distinct 100.7 MB caches
+rotate and every call reads K/V that is not in the 126 MB L2.
+
+Reported (one JSON line on rank 0):
+  value      algorithmic GB/s of the whole step with inputs resident in HBM, timed with CUDA events
+             around K replays of a CUDA graph of the step (15 kernels)
+  roofline   the split-attention kernel alone: its algorithmic bytes (K/V extent + Q) over its mean
+             CUDA-event duration, against the measured HBM copy bandwidth
+  e2e        the same metric through the C ABI with host buffers: per call the H2D copy of q, the new
+             K/V rows and the positions from pinned memory and the D2H copy of the output, inside the
+             timed region, one synchronisation per step
+  cpu_baseline  the FP64 oracle on the host cores (rank 0, N = 1 only)
+``--impl reference`` times the oracle itself as the reference arm (bounded sample per step).
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import io
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verify-attn µs/call and achieved HBM GB/s vs GB300 peak, 1K–192K ctx, 1 GPU"
+CTX = 196608
+CAPACITY = 196672
+N_LIVES = (4, 5, 6, 7, 8)
+Q_BYTES = 8 * 6 * 128 * 2
+OUT_BYTES = 8 * 6 * 128 * 2
+
+
+def call_bytes(hi: int, n_live: int) -> int:
+    """Algorithmic bytes of one call: the K/V extent, q, the output, the new rows (read + written)."""
+    return 512 * hi + Q_BYTES + OUT_BYTES + 2 * 512 * n_live + 6 * 4
+
+
+def attn_kernel_bytes(hi: int) -> int:
+    """Algorithmic bytes of one split-attention launch: the K/V extent it must read, and q."""
+    return 512 * hi + Q_BYTES
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--splits", type=int, default=0, help="split count (0 = library policy)")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- distributed control
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group("gloo", rank=self.rank, world_size=self.world)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def aggregate(per_rank_units: float, per_rank_seconds: float, dist: Dist):
+    """Whole-job throughput: all ranks' units over the slowest rank's time (weak scaling)."""
+    t = dist.max(per_rank_seconds)
+    return per_rank_units * dist.world / t, t
+
+
+# ----------------------------------------------------------------------------- clocks
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for r in csv.reader(io.StringIO(open(self.path).read())):
+            if len(r) < 9:
+                continue
+            try:
+                rows.append(dict(sm=float(r[1]), max=float(r[2]), power=float(r[3]),
+                                 hw=r[5].strip(), hwt=r[6].strip(), swt=r[7].strip(), cap=r[8].strip()))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        busy = [x for x in rows if x["power"] > 0.3 * max(y["power"] for y in rows)] or rows
+        reasons = set()
+        for x in busy:
+            for k, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                            ("swt", "sw_thermal_slowdown"), ("cap", "sw_power_cap")):
+                if x[k].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(x["sm"] for x in busy), "sm_max_mhz": max(x["max"] for x in rows),
+                "reasons": sorted(reasons), "samples": len(busy)}
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- oracle timing
+def oracle_step_time(w, n_threads: int, min_seconds: float, max_reps: int = 1000):
+    import oracle
+    from speculative_decode_verify_gb300 import synth
+    qb, kb, vb = synth.bits(w.q).numpy(), synth.bits(w.k_hist).numpy(), synth.bits(w.v_hist).numpy()
+    oracle.verify_attn(qb, kb[:64], vb[:64], [0] * w.n_rows, 1, w.sink.numpy(), w.scale, 0, n_threads=1)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.verify_attn(qb, kb, vb, w.pos.numpy(), w.n_live, w.sink.numpy(), w.scale, 0, n_threads=n_threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            return el / reps, reps
+
+
+def cpu_baseline(w_full):
+    cores = os.cpu_count() or 1
+    per_call, reps = oracle_step_time(w_full, cores, 10.0)
+    hi = int(w_full.pos[w_full.n_live - 1]) + 1
+    return {"value": call_bytes(hi, w_full.n_live) / per_call / 1e9, "unit": "GB/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{reps} full calls of the 196,608-position, n_live={w_full.n_live} workload "
+                      f"(all 48 row-head pairs, FP64), {cores} threads, {per_call * 1e3:.1f} ms/call"}
+
+
+def reference_arm(args, dist: Dist):
+    if dist.rank != 0:
+        return
+    from speculative_decode_verify_gb300 import synth
+    # bounded sample per step: the same verify call (8 rows, 48 row-head pairs, FP64) over a
+    # 4,096-position prefix of the synthetic history
+    w = synth.full_192k(8)
+    w.k_hist, w.v_hist = w.k_hist[:4096].clone(), w.v_hist[:4096].clone()
+    w.pos = synth.tail_positions(4096, 8)
+    cores = os.cpu_count() or 1
+    for _ in range(max(args.warmup, 1)):
+        oracle_step_time(w, cores, 0.0, 1)
+    t0 = time.perf_counter()
+    per, _ = oracle_step_time(w, cores, 0.0, args.steps)
+    total = time.perf_counter() - t0
+    bytes_step = call_bytes(4096, 8)
+    value = bytes_step * args.steps / total / 1e9
+    sample = (f"per step one FP64 oracle call: 8 rows x 6 heads over a 4,096-position prefix of the 196,608-"
+              f"position history, {cores} threads")
+    print(json.dumps({"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+                      "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
+                      "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                      "data": "synthetic",
+                      "config": {"workload": "full attention verify call, 1 KV head / 6 q heads, d 128, 8 rows "
+                                             "(oracle sample: 4,096-position prefix)"},
+                      "cpu_baseline": {"value": value, "unit": "GB/s", "kind": "oracle", "cores": cores,
+                                       "sample": sample},
+                      "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def ours(args, dist: Dist):
+    import ctypes
+
+    import torch
+
+    import speculative_decode_verify_gb300 as va
+    from speculative_decode_verify_gb300 import build as vbuild
+    from speculative_decode_verify_gb300 import synth
+
+    vbuild.build()
+    L = va.lib()
+    torch.cuda.set_device(dist.local_rank)
+    dev = torch.device("cuda", dist.local_rank)
+    stream = torch.cuda.Stream(dev)
+    S = args.splits or va.va_auto_splits(CTX, 0)
+
+    calls = []
+    w8 = None
+    for n in N_LIVES:
+        w = synth.full_192k(n)
+        if n == 8:
+            w8 = w
+        k = torch.full((CAPACITY, 128), synth.BF16_NAN, dtype=torch.int16, device=dev)
+        v = torch.full((CAPACITY, 128), synth.BF16_NAN, dtype=torch.int16, device=dev)
+        k[:CTX] = synth.bits(w.k_hist).to(dev)
+        v[:CTX] = synth.bits(w.v_hist).to(dev)
+        idx = w.pos[:n].to(torch.int64)
+        c = dict(n=n, k=k, v=v, hi=int(w.pos[n - 1]) + 1,
+                 q_h=synth.bits(w.q).pin_memory(), kn_h=synth.bits(w.k_hist)[idx].contiguous().pin_memory(),
+                 vn_h=synth.bits(w.v_hist)[idx].contiguous().pin_memory(), pos_h=w.pos.clone().pin_memory())
+        c["q"], c["kn"], c["vn"], c["pos"] = (c["q_h"].to(dev), c["kn_h"].to(dev), c["vn_h"].to(dev),
+                                             c["pos_h"].to(dev))
+        c["sink"] = w.sink.to(dev)
+        c["out"] = torch.empty(8, 6, 128, dtype=torch.int16, device=dev)
+        c["out_lse"] = torch.empty(8, 6, dtype=torch.float32, device=dev)
+        c["out_h"] = torch.empty(8, 6, 128, dtype=torch.int16).pin_memory()
+        c["out_lse_h"] = torch.empty(8, 6, dtype=torch.float32).pin_memory()
+        c["scale"] = w.scale
+        calls.append(c)
+    part_o = torch.empty(S, 8, 6, 128, dtype=torch.float32, device=dev)
+    part_lse = torch.empty(S, 8, 6, dtype=torch.float32, device=dev)
+    del w
+    torch.cuda.synchronize(dev)
+
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    P = ctypes.c_void_p
+
+    def launch_call(c, ev=None):
+        # the three C-ABI calls of one verify call, raw pointers prepared once per call
+        st = L.kv_ring_append(P(c["kn"].data_ptr()), P(c["vn"].data_ptr()), c["n"], P(c["k"].data_ptr()),
+                              P(c["v"].data_ptr()), CAPACITY, P(c["pos"].data_ptr()), None, sp)
+        if ev is not None:
+            ev[0].record(stream)
+        st |= L.verify_attn_full(P(c["q"].data_ptr()), 8, c["n"], P(c["k"].data_ptr()), P(c["v"].data_ptr()),
+                                 CAPACITY, P(c["pos"].data_ptr()), ctypes.c_float(c["scale"]), S,
+                                 P(part_o.data_ptr()), P(part_lse.data_ptr()), None, None, sp)
+        if ev is not None:
+            ev[1].record(stream)
+        st |= L.attn_split_combine(P(part_o.data_ptr()), P(part_lse.data_ptr()), S, P(c["sink"].data_ptr()), 8,
+                                   c["n"], P(c["out"].data_ptr()), P(c["out_lse"].data_ptr()), sp)
+        if st:
+            raise RuntimeError(f"verify call failed with status {st}")
+
+    def step():
+        for c in calls:
+            launch_call(c)
+
+    clocks = Clocks(dist.local_rank)
+    clocks.start()
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 3)):
+            step()
+        stream.synchronize()
+        # ---- value: K replays of a CUDA graph of the step (inputs resident in HBM)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step()
+        for _ in range(3):
+            g.replay()
+        stream.synchronize()
+        dist.barrier()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(stream)
+        e1.synchronize()
+        torch.cuda.synchronize(dev)
+        dist.barrier()
+        t_graph = e0.elapsed_time(e1) / 1e3
+        # ---- roofline: the split-attention kernel alone, events on its stream around each launch
+        kb = min(args.steps, 400)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(kb * len(calls))]
+        i = 0
+        for _ in range(kb):
+            for c in calls:
+                torch.cuda._sleep(100_000)      # keeps the GPU behind the host: no launch gap in the pair
+                launch_call(c, evs[i])
+                i += 1
+        stream.synchronize()
+        attn_s = [a.elapsed_time(b) / 1e3 for a, b in evs]
+        # ---- e2e: host buffers, copies inside the timed region, one synchronisation per step
+        h2d = sum(c["q_h"].numel() * 2 + c["kn_h"].numel() * 2 + c["vn_h"].numel() * 2 + c["pos_h"].numel() * 4
+                  for c in calls)
+        d2h = sum(c["out_h"].numel() * 2 + c["out_lse_h"].numel() * 4 for c in calls)
+        ke = args.steps
+        dist.barrier()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(ke):
+            for c in calls:
+                c["q"].copy_(c["q_h"], non_blocking=True)
+                c["kn"].copy_(c["kn_h"], non_blocking=True)
+                c["vn"].copy_(c["vn_h"], non_blocking=True)
+                c["pos"].copy_(c["pos_h"], non_blocking=True)
+                launch_call(c)
+                c["out_h"].copy_(c["out"], non_blocking=True)
+                c["out_lse_h"].copy_(c["out_lse"], non_blocking=True)
+            stream.synchronize()
+        t_e2e = time.perf_counter() - t0
+        dist.barrier()
+    clk = clocks.stop()
+
+    step_bytes = sum(call_bytes(c["hi"], c["n"]) for c in calls)
+    value, t_max = aggregate(step_bytes * args.steps / 1e9, t_graph, dist)
+    e2e_value, _ = aggregate(step_bytes * ke / 1e9, t_e2e, dist)
+    mean_attn = statistics.fmean(attn_s)
+    attn_bytes = statistics.fmean(attn_kernel_bytes(c["hi"]) for c in calls)
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    achieved = attn_bytes / mean_attn / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "full-attention verify, 196,608 positions (100.7 MB bf16 K/V), 1 KV head / 6 q "
+                               "heads, d 128, 8 rows with n_live 4,5,6,7,8 (one call each per step)",
+                   "calls_per_step": len(calls), "n_splits": S, "capacity": CAPACITY,
+                   "l2": "5 distinct 100.7 MB caches rotate: each call reads K/V untouched for ~400 MB of "
+                         "traffic, larger than L2 (no flush)",
+                   "timing": "CUDA graph of the step replayed K times, CUDA events on its stream",
+                   "parallelism": f"replicas x{dist.world} (one KV head per GPU, no collective)"},
+        "us_per_call": t_max / args.steps / len(calls) * 1e6,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": "verify_attn_full split kernel",
+                     "us_per_launch": mean_attn * 1e6, "launches": len(attn_s),
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs" if peaks else "fallback 6.8 TB/s"},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "us_per_step": t_e2e / ke * 1e6},
+        "gpu_launches": 3 * len(calls) * args.steps,
+        "clocks": clk,
+    }
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w8)
+    if dist.rank == 0:
+        print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            reference_arm(args, dist)
+        else:
+            ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

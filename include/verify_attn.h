@@ -1,0 +1,181 @@
+/*
+ * verify_attn.h - C ABI of the GB300 (sm_103a) speculative-decoding verify-attention library.
+ *
+ * One rank's share of a decode step's verification attention: one KV head serves six query
+ * heads (head_dim 128); up to eight verify rows (one committed token plus drafts, the rest
+ * padding) are folded with the six heads into 48 matrix rows that share every K/V tile; the
+ * history is partitioned along the sequence (split-KV) and the split partials are merged by a
+ * separate log-sum-exp combine.
+ *   Source: IQuestRT technical report, sections "Read only the KV tiles needed by the current
+ *   positions" (48-row folding, sequence partition, valid extent, causal boundary, zero-value
+ *   sink, separate combine, sliding-window ring of the window plus one 64-slot tile written
+ *   before it is read) and "Expose more parallelism in attention" (split-KV partials merged with
+ *   their log-sum-exp values, sink correction inside the combine).
+ *
+ * Conventions shared by every call
+ *   - bf16 data is passed as raw bit patterns (va_bf16).  All tensors are dense, row-major and
+ *     contiguous; every pointer named "device" must be a CUDA device (or managed) address.  The
+ *     q, K/V, new-row, partial and output buffers must be 16-byte aligned (VA_INVALID_ARG
+ *     otherwise); pos, sink, out_lse and dev_status need only their element alignment.
+ *   - Positions are 0-based absolute token positions, int32, in DEVICE memory so that a call can
+ *     be captured in a CUDA graph.  Verify row r sits at pos[r]; rows r < n_live are live; the
+ *     remaining rows up to n_rows are padding: their outputs are exactly 0 and their LSEs -inf.
+ *     Live positions must be non-decreasing (consecutive for a chain of drafts).
+ *   - A row at position p sees keys j <= p (full attention) or p - window < j <= p (sliding
+ *     window).  The read extent is [lo, hi) with hi = pos[n_live-1] + 1 and lo = 0 (full) or
+ *     max(0, pos[0] - window + 1) (sliding window): capacity beyond it is never read.
+ *   - Matrix row m = r * 6 + h (row r, query head h), i.e. q's own [n_rows][6][128] order.
+ *   - Sequence splits: 64-position tiles aligned to absolute position.  With t_lo = lo / 64,
+ *     t_hi = ceil(hi / 64) - 1 and T = t_hi - t_lo + 1, split s owns tiles
+ *     [t_lo + floor(s*T/S), t_lo + floor((s+1)*T/S)).  Splits that own no tile (S > T) write
+ *     o = 0 and lse = -inf.
+ *   - Ownership: the caller owns all memory; no call allocates, frees or synchronizes.  Every
+ *     call is asynchronous on `stream` (NULL = the legacy default stream); calls on one stream
+ *     run in order, which is what puts a ring append before the reads that need it.
+ *   - Errors: each call returns a va_status and launches nothing unless it returns VA_OK.
+ *     VA_CUDA_ERROR means a CUDA launch error was reported (cudaGetLastError).  Errors that
+ *     depend on device-resident positions are reported through the optional device word
+ *     `dev_status` (bits VA_DEV_*, OR-ed in; the caller clears it); the affected call then
+ *     writes empty partials.  No kernel traps, asserts or spins.
+ */
+#ifndef VERIFY_ATTN_H
+#define VERIFY_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define VA_API __attribute__((visibility("default")))
+#else
+#define VA_API
+#endif
+
+typedef uint16_t va_bf16;               /* raw bfloat16 bits */
+typedef struct CUstream_st *va_stream;  /* the same type as cudaStream_t */
+typedef int va_status;
+
+#define VA_OK 0
+#define VA_INVALID_ARG 1      /* null pointer, size out of range, non-finite scale ... */
+#define VA_UNSUPPORTED 2      /* a shape this library is not built for (ring_slots % 64 != 0) */
+#define VA_RING_TOO_SMALL 3   /* ring_slots < window + n_live - 1: appends would evict history */
+#define VA_CUDA_ERROR 4       /* a CUDA error was reported when launching */
+
+#define VA_HEAD_DIM 128       /* head dimension d */
+#define VA_Q_HEADS 6          /* query heads per KV head */
+#define VA_MAX_ROWS 8         /* verify rows per call (one committed token + up to 7 drafts) */
+#define VA_TILE 64            /* positions per K/V tile and split granule */
+#define VA_MAX_SPLITS 4096    /* largest accepted split count */
+
+/* device status bits (dev_status) */
+#define VA_DEV_NEGATIVE_POS 1     /* a live position is < 0 */
+#define VA_DEV_NOT_MONOTONE 2     /* live positions decrease */
+#define VA_DEV_BEYOND_CACHE 4     /* full attention: pos[n_live-1] >= capacity */
+#define VA_DEV_RING_SPAN 8        /* sliding window: pos[n_live-1] - pos[0] > ring_slots - window */
+
+/*
+ * kv_ring_append - write the live rows' new K and V into the cache before they are read.
+ * Source: IQuestRT report, "Read only the KV tiles needed by the current positions" (the
+ * sliding-window ring; verification writes its KV rows before reading them) and "Let correctness
+ * checks change the design" (ring of window + one 64-slot tile).
+ *   k_new, v_new  device [n_live][128] bf16: the new rows, row r for position pos[r]
+ *   n_live        0..8 (0: nothing is written)
+ *   k_cache, v_cache  device [slots][128] bf16, updated in place
+ *   slots         rows of the cache: the ring size for a sliding-window layer, the capacity for a
+ *                 full-attention layer; row r goes to slot pos[r] mod slots
+ *   pos           device int32 [>= n_live]
+ *   dev_status    optional device int32 (NULL = none): VA_DEV_NEGATIVE_POS for a negative
+ *                 position, whose row is then not written
+ * Returns VA_OK, VA_INVALID_ARG (null pointers with n_live > 0, n_live outside 0..8,
+ * slots < 1) or VA_CUDA_ERROR.
+ */
+VA_API va_status kv_ring_append(const va_bf16 *k_new, const va_bf16 *v_new, int n_live,
+                         va_bf16 *k_cache, va_bf16 *v_cache, int slots,
+                         const int32_t *pos, int32_t *dev_status, va_stream stream);
+
+/*
+ * verify_attn_full - split-KV verify attention of a full-attention layer.
+ * Source: IQuestRT report, "Read only the KV tiles needed by the current positions" (48 matrix
+ * rows, sequence partition, read extent from the current positions, causal mask at the
+ * boundary) and "Expose more parallelism in attention" (partials carry their LSE).
+ *   q             device [n_rows][6][128] bf16
+ *   n_rows        1..8; n_live 0..n_rows
+ *   k_cache, v_cache  device [capacity][128] bf16; row j holds absolute position j.  Rows at and
+ *                 beyond the extent are never read (they may hold anything, NaN included).
+ *   pos           device int32 [n_rows]
+ *   scale         softmax scale applied to q.k (finite; 1/sqrt(128) for this model)
+ *   n_splits      1..VA_MAX_SPLITS, or 0 = va_auto_splits(capacity, 0)
+ *   part_o        device float [n_splits][n_rows][6][128]: per split sum_j exp(s_j - lse_s) v_j
+ *                 (0 where the split sees nothing)
+ *   part_lse      device float [n_splits][n_rows][6]: per split ln sum_j exp(s_j) (natural log,
+ *                 post-scale scores; -inf where the split sees nothing).  No sink here.
+ *   splits_used   optional HOST int (NULL = none): receives the split count launched
+ *   dev_status    optional device int32: VA_DEV_NEGATIVE_POS / NOT_MONOTONE / BEYOND_CACHE
+ * Returns VA_OK, VA_INVALID_ARG or VA_CUDA_ERROR.
+ */
+VA_API va_status verify_attn_full(const va_bf16 *q, int n_rows, int n_live,
+                           const va_bf16 *k_cache, const va_bf16 *v_cache, int capacity,
+                           const int32_t *pos, float scale, int n_splits,
+                           float *part_o, float *part_lse, int *splits_used,
+                           int32_t *dev_status, va_stream stream);
+
+/*
+ * verify_attn_swa - split-KV verify attention of a sliding-window layer read from its ring.
+ * Source: IQuestRT report, "Read only the KV tiles needed by the current positions" (separate
+ * sliding-window path; ring of the window plus one 64-slot tile; every live row sees its
+ * complete window).  Call kv_ring_append for the same rows first, on the same stream.
+ *   As verify_attn_full, except:
+ *   k_ring, v_ring  device [ring_slots][128] bf16; position p lives in slot p mod ring_slots
+ *   ring_slots    a multiple of 64 (else VA_UNSUPPORTED), at least window + n_live - 1 (else
+ *                 VA_RING_TOO_SMALL); 4,160 for a 4,096 window
+ *   window        W >= 1: a row at p sees positions max(0, p - W + 1) .. p
+ *   n_splits      0 = va_auto_splits(window + n_live - 1, window)
+ *   dev_status    also VA_DEV_RING_SPAN if pos[n_live-1] - pos[0] > ring_slots - window
+ */
+VA_API va_status verify_attn_swa(const va_bf16 *q, int n_rows, int n_live,
+                          const va_bf16 *k_ring, const va_bf16 *v_ring, int ring_slots, int window,
+                          const int32_t *pos, float scale, int n_splits,
+                          float *part_o, float *part_lse, int *splits_used,
+                          int32_t *dev_status, va_stream stream);
+
+/*
+ * attn_split_combine - merge split partials by log-sum-exp and fold in the learned sink.
+ * Source: IQuestRT report, "Read only the KV tiles needed by the current positions" (a separate
+ * combine kernel issues the partial loads together and keeps four independent FP32
+ * accumulation chains) and "Expose more parallelism in attention" (the combine applies the
+ * sink correction and keeps the BF16 rounding boundaries).
+ *   part_o, part_lse  device, as written by verify_attn_full / verify_attn_swa
+ *   n_splits      0..VA_MAX_SPLITS
+ *   sink          device float [6] (NULL = no sink): logit of a zero-value key, post-scale
+ *   n_rows, n_live as for the attention call
+ *   out           device [n_rows][6][128] bf16: sum_s exp(lse_s - L) o_s rounded once to bf16
+ *                 (nearest, ties to even), L = logsumexp({lse_s} U {sink_h}); padding rows 0
+ *   out_lse       optional device float [n_rows][6]: L (-inf for padding rows)
+ * Returns VA_OK, VA_INVALID_ARG or VA_CUDA_ERROR.
+ */
+VA_API va_status attn_split_combine(const float *part_o, const float *part_lse, int n_splits,
+                             const float *sink, int n_rows, int n_live,
+                             va_bf16 *out, float *out_lse, va_stream stream);
+
+/* Bytes of one workspace holding part_o followed by part_lse for n_splits splits and 8 rows
+ * (part_lse then starts at n_splits * 8 * 6 * 128 floats).  0 if n_splits is out of range. */
+VA_API size_t va_workspace_bytes(int n_splits);
+
+/* Split count for a call whose extent is about extent_hint positions (window > 0: sliding
+ * window layer), chosen for the current device's SM count.  Host only; never launches. */
+VA_API int va_auto_splits(int extent_hint, int window);
+
+/* The same policy for an explicit SM count (no device query; usable without a GPU). */
+VA_API int va_auto_splits_for(int extent_hint, int window, int sm_count);
+
+/* Name of a va_status value. */
+VA_API const char *va_status_string(va_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VERIFY_ATTN_H */

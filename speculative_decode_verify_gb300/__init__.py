@@ -1,1 +1,144 @@
-"""GB300-native speculative-decoding verify attention (placeholder; binding added next)."""
+"""GB300-native speculative-decoding verify attention.
+
+Thin ctypes binding over the C ABI of ``libverify_attn.so`` (declared in
+``include/verify_attn.h``): every function here only marshals torch tensors into pointers and
+sizes and calls the entry point of the same name; all the work runs in the library's CUDA
+kernels.  There is no CPU fallback: if the compiled library is missing, every call raises.
+
+Source: IQuestRT technical report, sections "Read only the KV tiles needed by the current
+positions" and "Expose more parallelism in attention".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "VerifyAttnError", "lib", "lib_path", "kv_ring_append", "verify_attn_full", "verify_attn_swa",
+    "attn_split_combine", "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string",
+    "HEAD_DIM", "Q_HEADS", "MAX_ROWS", "TILE", "MAX_SPLITS", "EXPORTS",
+    "VA_OK", "VA_INVALID_ARG", "VA_UNSUPPORTED", "VA_RING_TOO_SMALL", "VA_CUDA_ERROR",
+]
+
+HEAD_DIM, Q_HEADS, MAX_ROWS, TILE, MAX_SPLITS = 128, 6, 8, 64, 4096
+VA_OK, VA_INVALID_ARG, VA_UNSUPPORTED, VA_RING_TOO_SMALL, VA_CUDA_ERROR = 0, 1, 2, 3, 4
+EXPORTS = ("kv_ring_append", "verify_attn_full", "verify_attn_swa", "attn_split_combine",
+           "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string")
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_lib = {}
+_lock = threading.Lock()
+
+
+class VerifyAttnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} returned {va_status_string(status)} ({status})")
+
+
+def lib_path(variant: str = "") -> str:
+    return os.path.join(_PKG, "_build", f"libverify_attn{variant}.so")
+
+
+def lib(variant: str = "") -> ctypes.CDLL:
+    """The loaded CUDA library (built by ``speculative_decode_verify_gb300.build``)."""
+    with _lock:
+        if variant in _lib:
+            return _lib[variant]
+        path = lib_path(variant)
+        if not os.path.exists(path):
+            raise RuntimeError(f"CUDA library not built ({path}); run speculative_decode_verify_gb300.build.build()")
+        L = ctypes.CDLL(path)
+        p, i, f = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        L.kv_ring_append.argtypes = [p, p, i, p, p, i, p, p, p]
+        L.verify_attn_full.argtypes = [p, i, i, p, p, i, p, f, i, p, p, ctypes.POINTER(i), p, p]
+        L.verify_attn_swa.argtypes = [p, i, i, p, p, i, i, p, f, i, p, p, ctypes.POINTER(i), p, p]
+        L.attn_split_combine.argtypes = [p, p, i, p, i, i, p, p, p]
+        for fn in ("kv_ring_append", "verify_attn_full", "verify_attn_swa", "attn_split_combine"):
+            getattr(L, fn).restype = i
+        L.va_workspace_bytes.argtypes = [i]
+        L.va_workspace_bytes.restype = ctypes.c_size_t
+        L.va_auto_splits.argtypes = [i, i]
+        L.va_auto_splits.restype = i
+        L.va_auto_splits_for.argtypes = [i, i, i]
+        L.va_auto_splits_for.restype = i
+        L.va_status_string.argtypes = [i]
+        L.va_status_string.restype = ctypes.c_char_p
+        _lib[variant] = L
+        return L
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn: str, status: int) -> None:
+    if status != VA_OK:
+        raise VerifyAttnError(fn, status)
+
+
+def va_status_string(status: int) -> str:
+    return lib().va_status_string(int(status)).decode()
+
+
+def va_workspace_bytes(n_splits: int) -> int:
+    return int(lib().va_workspace_bytes(int(n_splits)))
+
+
+def va_auto_splits(extent_hint: int, window: int = 0) -> int:
+    return int(lib().va_auto_splits(int(extent_hint), int(window)))
+
+
+def va_auto_splits_for(extent_hint: int, window: int, sm_count: int) -> int:
+    return int(lib().va_auto_splits_for(int(extent_hint), int(window), int(sm_count)))
+
+
+def kv_ring_append(k_new, v_new, n_live: int, k_cache, v_cache, pos, dev_status=None, stream=None,
+                   variant: str = "") -> None:
+    """Write the live rows' K/V ([n_live,128] bf16) to slot pos[r] mod slots of the cache."""
+    st = lib(variant).kv_ring_append(_ptr(k_new), _ptr(v_new), int(n_live), _ptr(k_cache), _ptr(v_cache),
+                                     int(k_cache.shape[0]), _ptr(pos), _ptr(dev_status), _stream(stream))
+    _check("kv_ring_append", st)
+
+
+def verify_attn_full(q, n_live: int, k_cache, v_cache, pos, scale: float, part_o, part_lse,
+                     n_splits: int = 0, dev_status=None, stream=None, variant: str = "") -> int:
+    """Split-KV attention of a full-attention layer; returns the split count launched."""
+    used = ctypes.c_int(0)
+    st = lib(variant).verify_attn_full(_ptr(q), int(q.shape[0]), int(n_live), _ptr(k_cache), _ptr(v_cache),
+                                       int(k_cache.shape[0]), _ptr(pos), float(scale), int(n_splits),
+                                       _ptr(part_o), _ptr(part_lse), ctypes.byref(used), _ptr(dev_status),
+                                       _stream(stream))
+    _check("verify_attn_full", st)
+    return used.value
+
+
+def verify_attn_swa(q, n_live: int, k_ring, v_ring, window: int, pos, scale: float, part_o, part_lse,
+                    n_splits: int = 0, dev_status=None, stream=None, variant: str = "") -> int:
+    """Split-KV attention of a sliding-window layer read from its ring; returns the split count."""
+    used = ctypes.c_int(0)
+    st = lib(variant).verify_attn_swa(_ptr(q), int(q.shape[0]), int(n_live), _ptr(k_ring), _ptr(v_ring),
+                                      int(k_ring.shape[0]), int(window), _ptr(pos), float(scale), int(n_splits),
+                                      _ptr(part_o), _ptr(part_lse), ctypes.byref(used), _ptr(dev_status),
+                                      _stream(stream))
+    _check("verify_attn_swa", st)
+    return used.value
+
+
+def attn_split_combine(part_o, part_lse, n_splits: int, sink, n_live: int, out, out_lse=None, stream=None,
+                       variant: str = "") -> None:
+    """Log-sum-exp merge of the partials with the sink; writes bf16 ``out`` [n_rows,6,128]."""
+    st = lib(variant).attn_split_combine(_ptr(part_o), _ptr(part_lse), int(n_splits), _ptr(sink),
+                                         int(out.shape[0]), int(n_live), _ptr(out), _ptr(out_lse),
+                                         _stream(stream))
+    _check("attn_split_combine", st)

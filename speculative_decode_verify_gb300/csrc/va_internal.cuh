@@ -1,0 +1,80 @@
+// Internal declarations shared by the library's translation units (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "verify_attn.h"
+
+namespace va {
+
+constexpr int kD = VA_HEAD_DIM;        // 128
+constexpr int kH = VA_Q_HEADS;         // 6
+constexpr int kMaxRows = VA_MAX_ROWS;  // 8
+constexpr int kTile = VA_TILE;         // 64
+constexpr int kMaxM = kH * kMaxRows;   // 48 matrix rows
+
+// Arguments of one split-KV attention launch (full attention: window == 0).
+struct AttnArgs {
+    const uint16_t* q;       // [n_rows][6][128] bf16
+    const uint16_t* k;       // [slots][128] bf16
+    const uint16_t* v;       // [slots][128] bf16
+    const int32_t* pos;      // [n_rows]
+    float* part_o;           // [S][n_rows][6][128]
+    float* part_lse;         // [S][n_rows][6]
+    int32_t* dev_status;     // optional
+    float scale;
+    int n_rows, n_live, slots, window, n_splits;
+};
+
+// Extent and split ownership derived on the device from the positions.
+// IQuestRT report, "Read only the KV tiles needed by the current positions": the current
+// positions determine the read extent; the sequence is partitioned across CTAs.
+struct Plan {
+    long long lo, hi;      // visible extent [lo, hi) of the live rows
+    long long t0, t1;      // this split's 64-position tiles [t0, t1)
+    int status;            // VA_DEV_* bits, 0 if the positions are usable
+};
+
+__device__ __forceinline__ Plan make_plan(const int32_t* __restrict__ pos, int n_live, int window,
+                                          int slots, int n_splits, int split) {
+    Plan P;
+    P.lo = P.hi = P.t0 = P.t1 = 0;
+    P.status = 0;
+    if (n_live <= 0) return P;
+    const int p0 = __ldg(pos);
+    int prev = p0, last = p0;
+    if (p0 < 0) P.status |= VA_DEV_NEGATIVE_POS;
+    for (int r = 1; r < n_live; ++r) {
+        const int p = __ldg(pos + r);
+        if (p < 0) P.status |= VA_DEV_NEGATIVE_POS;
+        if (p < prev) P.status |= VA_DEV_NOT_MONOTONE;
+        prev = p;
+        last = p;
+    }
+    if (window == 0 && (long long)last >= (long long)slots) P.status |= VA_DEV_BEYOND_CACHE;
+    if (window > 0 && (long long)last - p0 > (long long)slots - window) P.status |= VA_DEV_RING_SPAN;
+    if (P.status) return P;
+    P.hi = (long long)last + 1;
+    P.lo = window > 0 ? max(0LL, (long long)p0 - window + 1) : 0LL;
+    const long long tlo = P.lo / kTile;
+    const long long thi = (P.hi + kTile - 1) / kTile - 1;
+    const long long T = thi - tlo + 1;
+    P.t0 = tlo + (long long)split * T / n_splits;
+    P.t1 = tlo + (long long)(split + 1) * T / n_splits;
+    return P;
+}
+
+// Opt a kernel into `bytes` of dynamic shared memory on the current device, once per device
+// (so that a later launch under stream capture issues no attribute call).
+cudaError_t ensure_smem_attr(const void* kernel, int bytes);
+
+// Launchers (return the cudaError_t of the launch).
+cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, int n_live, uint16_t* k_cache,
+                          uint16_t* v_cache, int slots, const int32_t* pos, int32_t* dev_status,
+                          cudaStream_t stream);
+cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream);
+cudaError_t launch_combine(const float* part_o, const float* part_lse, int n_splits, const float* sink,
+                           int n_rows, int n_live, uint16_t* out, float* out_lse, cudaStream_t stream);
+
+}  // namespace va

@@ -1,0 +1,146 @@
+"""Host-side checks of the C ABI (no GPU needed, no kernel launched).
+
+The library must load, export every function include/verify_attn.h declares, reject bad
+arguments before launching anything, and agree with the shapes the pages state.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decode_verify_gb300 as va
+from speculative_decode_verify_gb300 import build as vbuild
+from speculative_decode_verify_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "verify_attn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    vbuild.build()
+    return va.lib()
+
+
+def _declared():
+    src = open(HEADER).read()
+    return re.findall(r"VA_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+
+
+def _defines():
+    src = open(HEADER).read()
+    return {k: int(v) for k, v in re.findall(r"#define\s+(VA_\w+)\s+(-?\d+)\b", src)}
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for n in ("kv_ring_append", "verify_attn_full", "verify_attn_swa", "attn_split_combine"):
+        assert n in names
+    assert set(names) == set(va.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for n in _declared():
+        assert hasattr(L, n), n
+
+
+def test_binding_constants_match_header():
+    d = _defines()
+    assert (d["VA_HEAD_DIM"], d["VA_Q_HEADS"], d["VA_MAX_ROWS"], d["VA_TILE"], d["VA_MAX_SPLITS"]) == \
+        (va.HEAD_DIM, va.Q_HEADS, va.MAX_ROWS, va.TILE, va.MAX_SPLITS)
+    assert (d["VA_OK"], d["VA_INVALID_ARG"], d["VA_UNSUPPORTED"], d["VA_RING_TOO_SMALL"], d["VA_CUDA_ERROR"]) == \
+        (va.VA_OK, va.VA_INVALID_ARG, va.VA_UNSUPPORTED, va.VA_RING_TOO_SMALL, va.VA_CUDA_ERROR)
+
+
+def test_page_constants_golden():
+    g = {}
+    for line in open(os.path.join(ROOT, "tests", "golden", "page_constants.txt")):
+        line = line.split("#")[0].strip()
+        if line:
+            k, v = line.split()
+            g[k] = int(v)
+    d = _defines()
+    assert d["VA_Q_HEADS"] == g["query_heads"] and d["VA_MAX_ROWS"] == g["verify_rows"]
+    assert d["VA_Q_HEADS"] * d["VA_MAX_ROWS"] == g["matrix_rows"]
+    assert synth.WINDOW == g["window"] and synth.RING_SLOTS == g["ring_slots"]
+    assert g["ring_slots"] == g["window"] + g["ring_extra_tile"] and d["VA_TILE"] == g["ring_extra_tile"]
+    # the enlarged ring keeps every live row's window when all eight rows are appended first
+    assert g["ring_slots"] >= g["window"] + g["verify_rows"] - 1
+    assert g["window"] < g["window"] + g["verify_rows"] - 1
+
+
+# fake, never-dereferenced addresses: every call below must be rejected before any launch
+FAKE = ctypes.c_void_p(0x1000)
+
+
+def _full(L, **kw):
+    a = dict(q=FAKE, n_rows=8, n_live=5, k=FAKE, v=FAKE, cap=1024, pos=FAKE, scale=0.088, S=4, po=FAKE, pl=FAKE)
+    a.update(kw)
+    return L.verify_attn_full(a["q"], a["n_rows"], a["n_live"], a["k"], a["v"], a["cap"], a["pos"], a["scale"],
+                              a["S"], a["po"], a["pl"], None, None, None)
+
+
+def _swa(L, **kw):
+    a = dict(q=FAKE, n_rows=8, n_live=8, k=FAKE, v=FAKE, R=4160, W=4096, pos=FAKE, scale=0.088, S=4,
+             po=FAKE, pl=FAKE)
+    a.update(kw)
+    return L.verify_attn_swa(a["q"], a["n_rows"], a["n_live"], a["k"], a["v"], a["R"], a["W"], a["pos"],
+                             a["scale"], a["S"], a["po"], a["pl"], None, None, None)
+
+
+@pytest.mark.parametrize("kw", [dict(q=None), dict(k=None), dict(pos=None), dict(po=None), dict(pl=None),
+                                dict(n_rows=0), dict(n_rows=9), dict(n_live=-1), dict(n_live=9),
+                                dict(cap=0), dict(S=-1), dict(S=4097), dict(scale=float("nan")),
+                                dict(scale=float("inf"))])
+def test_full_rejects_bad_arguments(L, kw):
+    assert _full(L, **kw) == va.VA_INVALID_ARG
+
+
+def test_misaligned_pointers_are_rejected(L):
+    odd = ctypes.c_void_p(0x1002)
+    assert _full(L, q=odd) == va.VA_INVALID_ARG
+    assert _full(L, k=odd) == va.VA_INVALID_ARG
+    assert _full(L, po=odd) == va.VA_INVALID_ARG
+    assert _swa(L, v=odd) == va.VA_INVALID_ARG
+    assert L.kv_ring_append(odd, FAKE, 2, FAKE, FAKE, 64, FAKE, None, None) == va.VA_INVALID_ARG
+    assert L.attn_split_combine(FAKE, FAKE, 4, None, 8, 8, odd, None, None) == va.VA_INVALID_ARG
+
+
+def test_swa_ring_checks(L):
+    assert _swa(L, R=4100) == va.VA_UNSUPPORTED                 # not a multiple of 64
+    assert _swa(L, R=4096) == va.VA_RING_TOO_SMALL              # the ring the pages fixed
+    assert _swa(L, R=4096, n_live=1, q=None) == va.VA_INVALID_ARG
+    assert _swa(L, W=0) == va.VA_INVALID_ARG
+    assert _swa(L, R=4160, n_live=8, W=4160 - 6) == va.VA_RING_TOO_SMALL   # needs W + 7 slots
+
+
+def test_append_and_combine_reject_bad_arguments(L):
+    assert L.kv_ring_append(FAKE, FAKE, 9, FAKE, FAKE, 64, FAKE, None, None) == va.VA_INVALID_ARG
+    assert L.kv_ring_append(FAKE, FAKE, 2, FAKE, FAKE, 0, FAKE, None, None) == va.VA_INVALID_ARG
+    assert L.kv_ring_append(None, FAKE, 2, FAKE, FAKE, 64, FAKE, None, None) == va.VA_INVALID_ARG
+    assert L.kv_ring_append(None, None, 0, None, None, 64, None, None, None) == va.VA_OK   # nothing to do
+    assert L.attn_split_combine(FAKE, FAKE, 4, None, 8, 8, None, None, None) == va.VA_INVALID_ARG
+    assert L.attn_split_combine(None, FAKE, 4, None, 8, 8, FAKE, None, None) == va.VA_INVALID_ARG
+    assert L.attn_split_combine(FAKE, FAKE, 4097, None, 8, 8, FAKE, None, None) == va.VA_INVALID_ARG
+    assert L.attn_split_combine(FAKE, FAKE, 4, None, 8, 9, FAKE, None, None) == va.VA_INVALID_ARG
+
+
+def test_workspace_and_status_strings(L):
+    assert va.va_workspace_bytes(0) == 0 and va.va_workspace_bytes(4097) == 0
+    assert va.va_workspace_bytes(152) == 4 * 152 * 8 * 6 * 129
+    assert va.va_status_string(va.VA_RING_TOO_SMALL) == "VA_RING_TOO_SMALL"
+    assert va.va_status_string(99) == "VA_UNKNOWN_STATUS"
+
+
+def test_auto_split_policy(L):
+    for sm in (148, 152):
+        assert va.va_auto_splits_for(196608, 0, sm) == sm          # long context fills every SM
+        prev = 0
+        for ext in (1, 64, 128, 1024, 4096, 16384, 65536, 196608, 1 << 30):
+            s = va.va_auto_splits_for(ext, 0, sm)
+            assert 1 <= s <= sm and s >= prev
+            prev = s
+        s_swa = va.va_auto_splits_for(4103, 4096, sm)
+        assert s_swa == va.va_auto_splits_for(10 ** 6, 4096, sm)   # a window bounds the work
+        assert 1 <= s_swa <= sm

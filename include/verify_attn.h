@@ -75,6 +75,7 @@ typedef int va_status;
 #define VA_DEV_NOT_MONOTONE 2     /* live positions decrease */
 #define VA_DEV_BEYOND_CACHE 4     /* full attention: pos[n_live-1] >= capacity */
 #define VA_DEV_RING_SPAN 8        /* sliding window: pos[n_live-1] - pos[0] > ring_slots - window */
+#define VA_DEV_TIMEOUT 16         /* a kernel gave up on a bounded wait; its outputs are not valid */
 
 /*
  * kv_ring_append - write the live rows' new K and V into the cache before they are read.

@@ -61,6 +61,11 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--splits", type=int, default=0, help="split count (0 = library policy)")
+    ap.add_argument("--kernel-only", action="store_true",
+                    help="profiling aid: only the split-attention launches, over --caches rotating caches")
+    ap.add_argument("--caches", type=int, default=5, help="distinct 192K caches to rotate (1..5)")
+    ap.add_argument("--variant", default="", help="library build variant to load (A/B tuning aid)")
+    ap.add_argument("--ctx", type=int, default=CTX, help="context of the --kernel-only runs")
     return ap.parse_args()
 
 
@@ -227,7 +232,7 @@ def ours(args, dist: Dist):
     from speculative_decode_verify_gb300 import synth
 
     vbuild.build()
-    L = va.lib()
+    L = va.lib(args.variant)
     torch.cuda.set_device(dist.local_rank)
     dev = torch.device("cuda", dist.local_rank)
     stream = torch.cuda.Stream(dev)
@@ -235,14 +240,19 @@ def ours(args, dist: Dist):
 
     calls = []
     w8 = None
-    for n in N_LIVES:
-        w = synth.full_192k(n)
+    n_lives = N_LIVES[len(N_LIVES) - max(1, min(args.caches, len(N_LIVES))):]
+    ctx = args.ctx if args.kernel_only else CTX
+    cap = ctx + 64
+    if args.kernel_only and not args.splits:
+        S = va.va_auto_splits(ctx, 0)
+    for n in n_lives:
+        w = synth.full_192k(n) if ctx == CTX else synth.make(f"ctx{ctx}", 4 + n, ctx=ctx, n_live=n, slots=cap)
         if n == 8:
             w8 = w
-        k = torch.full((CAPACITY, 128), synth.BF16_NAN, dtype=torch.int16, device=dev)
-        v = torch.full((CAPACITY, 128), synth.BF16_NAN, dtype=torch.int16, device=dev)
-        k[:CTX] = synth.bits(w.k_hist).to(dev)
-        v[:CTX] = synth.bits(w.v_hist).to(dev)
+        k = torch.full((cap, 128), synth.BF16_NAN, dtype=torch.int16, device=dev)
+        v = torch.full((cap, 128), synth.BF16_NAN, dtype=torch.int16, device=dev)
+        k[:ctx] = synth.bits(w.k_hist).to(dev)
+        v[:ctx] = synth.bits(w.v_hist).to(dev)
         idx = w.pos[:n].to(torch.int64)
         c = dict(n=n, k=k, v=v, hi=int(w.pos[n - 1]) + 1,
                  q_h=synth.bits(w.q).pin_memory(), kn_h=synth.bits(w.k_hist)[idx].contiguous().pin_memory(),
@@ -283,6 +293,31 @@ def ours(args, dist: Dist):
     def step():
         for c in calls:
             launch_call(c)
+
+    if args.kernel_only:
+        # the split-attention kernel alone, back to back over the rotating caches (for ncu captures)
+        with torch.cuda.stream(stream):
+            def attn(c):
+                st = L.verify_attn_full(P(c["q"].data_ptr()), 8, c["n"], P(c["k"].data_ptr()), P(c["v"].data_ptr()),
+                                        cap, P(c["pos"].data_ptr()), ctypes.c_float(c["scale"]), S,
+                                        P(part_o.data_ptr()), P(part_lse.data_ptr()), None, None, sp)
+                if st:
+                    raise RuntimeError(f"verify_attn_full failed with status {st}")
+            for _ in range(max(args.warmup, 1)):
+                for c in calls:
+                    attn(c)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                for c in calls:
+                    attn(c)
+            e1.record(stream)
+            e1.synchronize()
+        n = args.steps * len(calls)
+        us = e0.elapsed_time(e1) * 1e3 / n
+        print(json.dumps({"kernel_only": True, "variant": args.variant, "ctx": ctx, "launches": n,
+                          "us_per_launch": us, "n_splits": S, "gbs": attn_kernel_bytes(ctx) / us / 1e3}))
+        return
 
     clocks = Clocks(dist.local_rank)
     clocks.start()

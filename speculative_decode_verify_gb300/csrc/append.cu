@@ -1,6 +1,7 @@
 // Ring / cache append of the verify rows' new K and V.
 // IQuestRT report, "Read only the KV tiles needed by the current positions": verification writes
 // its KV rows before reading them; position p lives in slot p mod ring_slots.
+#include "tc_ptx.cuh"
 #include "va_internal.cuh"
 
 namespace va {
@@ -13,7 +14,9 @@ __global__ void __launch_bounds__(32) kv_append_kernel(const uint4* __restrict__
                                                        int32_t* dev_status) {
     const int r = blockIdx.x;
     const int lane = threadIdx.x;
-    const int p = __ldg(pos + r);
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // every global access comes after this
+    const int p = __ldcg(pos + r);
     if (p < 0) {
         if (lane == 0 && dev_status) atomicOr(dev_status, VA_DEV_NEGATIVE_POS);
         return;
@@ -22,19 +25,21 @@ __global__ void __launch_bounds__(32) kv_append_kernel(const uint4* __restrict__
     constexpr int kChunks = kD * 2 / 16;   // 16 chunks of 16 B per row
     const int c = lane & (kChunks - 1);
     if (lane < kChunks)
-        k_cache[slot * kChunks + c] = __ldg(k_new + (long long)r * kChunks + c);
+        k_cache[slot * kChunks + c] = __ldcg(k_new + (long long)r * kChunks + c);
     else
-        v_cache[slot * kChunks + c] = __ldg(v_new + (long long)r * kChunks + c);
+        v_cache[slot * kChunks + c] = __ldcg(v_new + (long long)r * kChunks + c);
 }
 
 cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, int n_live, uint16_t* k_cache,
                           uint16_t* v_cache, int slots, const int32_t* pos, int32_t* dev_status,
                           cudaStream_t stream) {
-    kv_append_kernel<<<n_live, 32, 0, stream>>>(reinterpret_cast<const uint4*>(k_new),
-                                                reinterpret_cast<const uint4*>(v_new),
-                                                reinterpret_cast<uint4*>(k_cache),
-                                                reinterpret_cast<uint4*>(v_cache), slots, pos, dev_status);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    pdl_config(&cfg, attr, dim3(n_live), dim3(32), 0, stream);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kv_append_kernel, reinterpret_cast<const uint4*>(k_new),
+                                             reinterpret_cast<const uint4*>(v_new), reinterpret_cast<uint4*>(k_cache),
+                                             reinterpret_cast<uint4*>(v_cache), slots, pos, dev_status);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace va

@@ -10,10 +10,15 @@
 //   * Transposed products so that the 128-row MMA dimension is always full: for a tile of 128 keys,
 //     S^T[128 keys x 48 rows] = K[128 x 128] . Q^T, and O^T[128 d x 48 rows] += V^T . P^T.  Both
 //     accumulators live in tensor memory (TMEM); S^T is double-buffered, O^T accumulates over tiles.
-//   * A TMA warp streams 64-position boxes of K and V (128-byte swizzle) into a 3-deep K ring and a
-//     2-deep V ring; K and V complete separate barriers, so QK starts as soon as K has landed.
-//   * One thread issues the MMAs; four softmax warps own one TMEM lane quadrant each: thread L holds
-//     key L of the tile for S^T and output column d = L for O^T.
+//   * Two TMA warps stream 64-position boxes of K and V (128-byte swizzle) into 3-deep K and V
+//     rings; K and V complete separate barriers, so QK starts as soon as K has landed.  Q and the first
+//     stages are requested before the CTA's own set-up, and every load also asks L2 for the tile
+//     kPrefetch tiles further on, so the rings refill from L2 rather than from DRAM.  P^T of a tile is written over that tile's K
+//     once QK has consumed it, so the P buffers cost no extra shared memory and are double-buffered.
+//   * One warp each issues the K loads, the V loads and the MMAs (one thread per role, so that a role
+//     waiting on a barrier never holds up another); eight softmax warps, two per TMEM lane quadrant (one
+//     per half of the 48 matrix rows): thread L holds key L of the tile for S^T and output column d = L
+//     for O^T.
 //   * Softmax keeps one reference maximum per matrix row, shared by the CTA.  Scores may exceed it by up
 //     to 2^8 before it is raised (a CTA-wide vote); raising it rescales the TMEM accumulator and the
 //     running sums.  The log-sum-exp stays exact: lse = ref + log2(sum) in base-2 units.
@@ -36,8 +41,30 @@
 namespace va {
 namespace tc {
 
-constexpr int kNK = 3;                    // K ring depth (tiles of 128 positions)
-constexpr int kNV = 2;                    // V ring depth
+#ifndef VA_NK
+#define VA_NK 4
+#endif
+#ifndef VA_NV
+#define VA_NV 2
+#endif
+#ifndef VA_ROTATE
+#define VA_ROTATE 0
+#endif
+// Start-up shaping: every CTA asks for its first tiles at the same moment and the DRAM serves all of
+// them interleaved, so tile 0 lands no earlier than the rest and no stage frees up for several us.
+// Requesting tile j of the first ring fill j * VA_STAGGER_NS after tile 0 lets tile 0 land first.
+// 1.2 us measured best on GB300 (0: no stagger).
+#ifndef VA_STAGGER_NS
+#define VA_STAGGER_NS 1200
+#endif
+constexpr int kNK = VA_NK;                // K ring depth (tiles of 128 positions); P of tile j reuses K's stage
+constexpr int kNV = VA_NV;                // V ring depth
+#ifndef VA_PREFETCH
+#define VA_PREFETCH 0
+#endif
+// Tiles requested into L2 ahead of the rings.  Off: the per-SM TMA engine that serves the rings also
+// serves the prefetches, and measured on GB300 every prefetch distance (2, 4, 6) made the kernel slower.
+constexpr int kPrefetch = VA_PREFETCH;
 constexpr uint32_t kHalfBox = 8192;       // one TMA box: 64 positions x 64 columns x 2 B
 constexpr uint32_t kDHalf = 16384;        // 128 positions x 64 columns: one column half of a stage
 constexpr uint32_t kStage = 32768;        // K or V of one 128-position tile
@@ -47,29 +74,36 @@ constexpr uint32_t kPBytes = 16384;       // P^T: 128 keys x 64 columns (48 used
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kOffK + kNK * kStage;
 constexpr uint32_t kOffQ = kOffV + kNV * kStage;
-constexpr uint32_t kOffPhi = kOffQ + kQBytes;
-constexpr uint32_t kOffPlo = kOffPhi + kPBytes;
-constexpr uint32_t kOffMisc = kOffPlo + kPBytes;
-constexpr int kThreads = 192;             // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 softmax
+constexpr uint32_t kOffMisc = kOffQ + kQBytes;
+// Once QK(j) has read K(j), its stage holds P^T of tile j: the hi part in the first 16 KB, the lo part
+// in the second.  The stage returns to the K ring when PV(j) has read P.
+constexpr uint32_t kPhiInStage = 0, kPloInStage = kPBytes;
+constexpr int kSoftWarps = 8;            // two per SM sub-partition: (lane quadrant, column half)
+constexpr int kSoftWarp0 = 3;                    // warp 0 K loads, warp 1 MMA + TMEM owner, warp 2 V loads
+constexpr int kThreads = 32 * (kSoftWarp0 + kSoftWarps);
+constexpr int kSoftThreads = 32 * kSoftWarps;
+constexpr int kCols = kMaxM / 2;          // matrix rows (accumulator columns) per softmax thread
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kColS0 = 0, kColS1 = 64, kColO = 128;
-constexpr float kThresh = 8.0f;           // log2 headroom above the reference maximum
+constexpr float kThresh = 256.0f;         // a probability may reach 2^8 before the reference is raised
 constexpr float kRefInit = -1.0e30f;      // reference maximum before any visible key
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 struct Misc {
     uint64_t k_full[kNK], k_empty[kNK], v_full[kNV], v_empty[kNV];
-    uint64_t s_full[2], s_free[2], p_full, pv_done, drain;
+    uint64_t q_full, s_full[2], s_free[2], p_full[2], pv_done, o_ready, drain;
     uint32_t tmem_base;
     int abort;
-    int vote[2][4];
+    int vote[2][kSoftWarps];
+    unsigned long long t_first;      // globaltimer when tile 0 was requested
     float red[4][kMaxM];
     float ref[kMaxM];
     float alpha[kMaxM];
+    float inv_l[kMaxM];
     long long row_lo[kMaxRows], row_hi[kMaxRows];
 };
 constexpr uint32_t kSmemBytes = kOffMisc + (uint32_t)sizeof(Misc) + 1024;
-static_assert(kOffQ % 1024 == 0 && kOffPhi % 1024 == 0 && kOffPlo % 1024 == 0, "swizzle atoms need 1 KB alignment");
+static_assert(kOffQ % 1024 == 0 && kStage % 1024 == 0 && 2 * kPBytes <= kStage, "swizzle atoms need 1 KB alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -79,15 +113,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return u;
 }
 
-// Column base of the three columns a lane holds after warp_reduce_scatter48.
+// Column base of the three columns a lane holds after warp_reduce_scatter24.
 __device__ __forceinline__ int scatter_col_base(int lane) {
-    return ((lane >> 4) & 1) * 24 + ((lane >> 3) & 1) * 12 + ((lane >> 2) & 1) * 6 + ((lane >> 1) & 1) * 3;
+    return ((lane >> 4) & 1) * 12 + ((lane >> 3) & 1) * 6 + ((lane >> 2) & 1) * 3;
 }
 
-// Reduce 48 per-thread columns over the warp; afterwards lane holds the warp totals of columns
-// [scatter_col_base(lane), +3) in v[0..2] (lanes 2i and 2i+1 hold the same three).
+// Reduce 24 per-thread columns over the warp; afterwards the lane holds the warp totals of columns
+// [scatter_col_base(lane), +3) in v[0..2] (the four lanes 4i..4i+3 hold the same three).
 template <bool kMax>
-__device__ __forceinline__ void warp_reduce_scatter48(float (&v)[48], int lane) {
+__device__ __forceinline__ void warp_reduce_scatter24(float (&v)[kCols], int lane) {
 #define VA_STAGE(W, BIT)                                                   \
     _Pragma("unroll") for (int i = 0; i < (W); ++i) {                      \
         const bool up = (lane & (BIT)) != 0;                               \
@@ -96,20 +130,36 @@ __device__ __forceinline__ void warp_reduce_scatter48(float (&v)[48], int lane) 
         const float got = __shfl_xor_sync(0xffffffffu, send, (BIT));       \
         v[i] = kMax ? fmaxf(keep, got) : keep + got;                       \
     }
-    VA_STAGE(24, 16)
-    VA_STAGE(12, 8)
-    VA_STAGE(6, 4)
-    VA_STAGE(3, 2)
+    VA_STAGE(12, 16)
+    VA_STAGE(6, 8)
+    VA_STAGE(3, 4)
 #undef VA_STAGE
 #pragma unroll
-    for (int i = 0; i < 3; ++i) {
-        const float got = __shfl_xor_sync(0xffffffffu, v[i], 1);
-        v[i] = kMax ? fmaxf(v[i], got) : v[i] + got;
-    }
+    for (int b = 2; b >= 1; b >>= 1)
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            const float got = __shfl_xor_sync(0xffffffffu, v[i], b);
+            v[i] = kMax ? fmaxf(v[i], got) : v[i] + got;
+        }
 }
 
+#ifdef VA_TRACE
+// Timeline probe of the debug build: per CTA, 256 globaltimer stamps (ns).  [0] start, [1] set-up
+// done, [2] end, [3] tile count; tile j (j < 31) at 8 + 8 j: K requested, V requested, K seen by the
+// MMA thread, V seen by the MMA thread, S seen by softmax, P published, P seen by the MMA thread.
+__device__ unsigned long long* g_trace = nullptr;
+#define VA_TRACE_AT(slot) \
+    do { if (g_trace && (slot) < 256) g_trace[(size_t)blockIdx.x * 256 + (slot)] = ptx::globaltimer_ns(); } while (0)
+#define VA_TRACE_TILE(j, k) do { if ((j) < 31) VA_TRACE_AT(8 + 8 * (j) + (k)); } while (0)
+#else
+#define VA_TRACE_AT(slot) do { } while (0)
+#define VA_TRACE_TILE(j, k) do { } while (0)
+#endif
+
 __global__ void __launch_bounds__(kThreads, 1)
-attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+               const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmk2,
+               const __grid_constant__ CUtensorMap tmv2) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw_s = ptx::smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
@@ -119,135 +169,209 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk, const 
     const int split = blockIdx.x;
     const int M = a.n_rows * kH;      // matrix rows present in q / the partials
     const int ML = a.n_live * kH;     // live matrix rows
+    if (tid == 0) VA_TRACE_AT(0);
+    auto bar = [](const uint64_t& b) { return ptx::smem_u32(&b); };
 
-    const Plan P = make_plan(a.pos, a.n_live, a.window, a.slots, a.n_splits, split);
+    // ---------------------------------------------------------------- set-up without global memory
+    if (tid == 0) {
+        ptx::mbar_init(bar(ms.q_full), 1);
+        for (int i = 0; i < kNK; ++i) {
+            ptx::mbar_init(bar(ms.k_full[i]), 1);
+            ptx::mbar_init(bar(ms.k_empty[i]), 1);
+        }
+        for (int i = 0; i < kNV; ++i) {
+            ptx::mbar_init(bar(ms.v_full[i]), 1);
+            ptx::mbar_init(bar(ms.v_empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(bar(ms.s_full[i]), 1);
+            ptx::mbar_init(bar(ms.s_free[i]), kSoftWarps);
+        }
+        ptx::mbar_init(bar(ms.p_full[0]), kSoftWarps);
+        ptx::mbar_init(bar(ms.p_full[1]), kSoftWarps);
+        ptx::mbar_init(bar(ms.pv_done), 1);
+        ptx::mbar_init(bar(ms.o_ready), 1);
+        ptx::mbar_init(bar(ms.drain), 1);
+        ms.abort = 0;
+        ptx::mbar_init_fence();
+    }
+    if (tid == 32) {
+        ptx::tma_prefetch_desc(&tmq);
+        ptx::tma_prefetch_desc(&tmk);
+        ptx::tma_prefetch_desc(&tmv);
+        ptx::tma_prefetch_desc(&tmk2);
+        ptx::tma_prefetch_desc(&tmv2);
+    }
+    if (warp == 1) ptx::tmem_alloc(ptx::smem_u32(&ms.tmem_base), kTmemCols);
+
+    // Programmatic dependent launch: every global access of this kernel comes after griddep_wait.
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
+
+    int row_pos[kMaxRows];
+    const Plan P = make_plan(a.pos, a.n_live, a.window, a.slots, a.n_splits, split, row_pos);
     if (P.status && split == 0 && tid == 0 && a.dev_status) atomicOr(a.dev_status, P.status);
     const int n64 = P.status ? 0 : (int)(P.t1 - P.t0);
     const int ntiles = (n64 + 1) >> 1;
     float* part_o = a.part_o + (long long)split * M * kD;
     float* part_lse = a.part_lse + (long long)split * M;
-    if (ntiles == 0) {  // empty split (or unusable positions): o = 0, lse = -inf
-        for (int i = tid; i < M * kD; i += kThreads) part_o[i] = 0.0f;
-        for (int i = tid; i < M; i += kThreads) part_lse[i] = -INFINITY;
-        return;
-    }
     const long long own_lo = max(P.lo, P.t0 * kTile);
     const long long own_hi = min(P.hi, P.t1 * kTile);
 
-    // ---------------------------------------------------------------- one-time set-up
-    if (tid < kMaxRows) {
-        long long lo = 0, hi = 0;
-        if (tid < a.n_live) {
-            const long long p = __ldg(a.pos + tid);
-            lo = a.window > 0 ? max(0LL, p - a.window + 1) : 0LL;
-            hi = p + 1;
-            lo = max(lo, own_lo);
-            hi = min(hi, own_hi);
-            if (hi < lo) hi = lo;
+    // Tile j covers 64-position tiles t = t0 + 2j and, unless it is the split's last odd tile, t + 1.
+    // Its cache rows start at slot(t); the two halves are contiguous unless a ring wraps between them.
+    // (VA_ROTATE: the CTA walks its tiles starting from a split-dependent one.)
+    const int rot = (VA_ROTATE && ntiles > 0) ? (int)((split * 7LL) % ntiles) : 0;
+    auto tile_t = [&](int j) { return P.t0 + 2LL * (VA_ROTATE ? (j + rot) % max(ntiles, 1) : j); };
+    auto tile_slots = [&](int j, int& slot0, int& slot1, int& halves) {
+        const long long t = tile_t(j);
+        halves = (t + 1 < P.t1) ? 2 : 1;
+        slot0 = (int)((t * kTile) % a.slots);
+        slot1 = (int)(((t + 1) * kTile) % a.slots);
+    };
+    // L2 prefetch of K or V of tile j (same boxes as the loads)
+    auto prefetch_tile = [&](const CUtensorMap* m64, const CUtensorMap* m128, int j) {
+        int s0, s1, halves;
+        tile_slots(j, s0, s1, halves);
+        if (halves == 2 && s1 == s0 + kTile) {
+            for (int h = 0; h < 2; ++h) ptx::tma_prefetch_l2_2d(m128, h * 64, s0);
+        } else {
+            for (int hh = 0; hh < halves; ++hh)
+                for (int h = 0; h < 2; ++h) ptx::tma_prefetch_l2_2d(m64, h * 64, hh ? s1 : s0);
         }
-        ms.row_lo[tid] = lo;
-        ms.row_hi[tid] = hi;
+    };
+    // K/V of tile j into its ring stage: per 64-column half one 128-row box (contiguous halves) or one
+    // 64-row box per half.  A load also prefetches tile j + kPrefetch into L2.
+    auto load_tile = [&](const CUtensorMap* m64, const CUtensorMap* m128, uint32_t stage, uint64_t& full, int j) {
+        int s0, s1, halves;
+        tile_slots(j, s0, s1, halves);
+        ptx::mbar_arrive_expect_tx(bar(full), (uint32_t)halves * 2u * kHalfBox);
+        if (halves == 2 && s1 == s0 + kTile) {
+            for (int h = 0; h < 2; ++h) ptx::tma_load_2d(stage + h * kDHalf, m128, h * 64, s0, bar(full));
+        } else {
+            for (int hh = 0; hh < halves; ++hh)
+                for (int h = 0; h < 2; ++h)
+                    ptx::tma_load_2d(stage + h * kDHalf + hh * kHalfBox, m64, h * 64, hh ? s1 : s0, bar(full));
+        }
+    };
+    auto load_k = [&](int j) {
+        VA_TRACE_TILE(j, 0);
+        load_tile(&tmk, &tmk2, base_s + kOffK + (uint32_t)(j % kNK) * kStage, ms.k_full[j % kNK], j);
+        if (kPrefetch > 0 && j >= kNK && j + kPrefetch < ntiles) prefetch_tile(&tmk, &tmk2, j + kPrefetch);
+    };
+    auto load_v = [&](int j) {
+        VA_TRACE_TILE(j, 1);
+        load_tile(&tmv, &tmv2, base_s + kOffV + (uint32_t)(j % kNV) * kStage, ms.v_full[j % kNV], j);
+        if (kPrefetch > 0 && j >= kNV && j + kPrefetch < ntiles) prefetch_tile(&tmv, &tmv2, j + kPrefetch);
+    };
+    // Initial fill: with VA_STAGGER_NS, only tile 0 is requested at once and the producers request
+    // tile j of the first ring fill j * VA_STAGGER_NS after it.
+    const int k_first = VA_STAGGER_NS ? min(1, ntiles) : min(kNK, ntiles);
+    const int v_first = VA_STAGGER_NS ? min(1, ntiles) : min(kNV, ntiles);
+    auto stagger = [&](int j) {
+        if (VA_STAGGER_NS == 0) return;
+        const unsigned long long due = ms.t_first + (unsigned long long)j * VA_STAGGER_NS;
+        for (int spin = 0; spin < 1000000 && ptx::globaltimer_ns() < due; ++spin) __nanosleep(64);
+    };
+
+    // ---------------------------------------------------------------- set-up with global memory
+    if (ntiles > 0) {
+        if (tid == 0) {
+            // Q, then the first stages
+            ptx::mbar_arrive_expect_tx(bar(ms.q_full), kQBytes);
+            ptx::tma_load_2d(base_s + kOffQ, &tmq, 0, 0, bar(ms.q_full));
+            ptx::tma_load_2d(base_s + kOffQ + kQHalf, &tmq, 64, 0, bar(ms.q_full));
+            ms.t_first = ptx::globaltimer_ns();
+            for (int j = 0; j < k_first; ++j) load_k(j);
+            for (int j = 0; j < v_first; ++j) load_v(j);
+        }
+        if (tid < kMaxRows) {
+            long long lo = 0, hi = 0;
+#pragma unroll
+            for (int r = 0; r < kMaxRows; ++r) {
+                if (r == tid && r < a.n_live) {
+                    const long long p = row_pos[r];
+                    lo = max(a.window > 0 ? max(0LL, p - a.window + 1) : 0LL, own_lo);
+                    hi = min(p + 1, own_hi);
+                    if (hi < lo) hi = lo;
+                }
+            }
+            ms.row_lo[tid] = lo;
+            ms.row_hi[tid] = hi;
+        }
+        if (tid < kMaxM) ms.ref[tid] = tid < ML ? kRefInit : INFINITY;   // padding rows never weigh anything
     }
-    if (tid < kMaxM) ms.ref[tid] = kRefInit;
-    if (warp == 1) ptx::tmem_alloc(ptx::smem_u32(&ms.tmem_base), kTmemCols);
-    if (tid == 0) {
-        for (int i = 0; i < kNK; ++i) {
-            ptx::mbar_init(ptx::smem_u32(&ms.k_full[i]), 1);
-            ptx::mbar_init(ptx::smem_u32(&ms.k_empty[i]), 1);
-        }
-        for (int i = 0; i < kNV; ++i) {
-            ptx::mbar_init(ptx::smem_u32(&ms.v_full[i]), 1);
-            ptx::mbar_init(ptx::smem_u32(&ms.v_empty[i]), 1);
-        }
-        for (int i = 0; i < 2; ++i) {
-            ptx::mbar_init(ptx::smem_u32(&ms.s_full[i]), 1);
-            ptx::mbar_init(ptx::smem_u32(&ms.s_free[i]), 4);
-        }
-        ptx::mbar_init(ptx::smem_u32(&ms.p_full), 4);
-        ptx::mbar_init(ptx::smem_u32(&ms.pv_done), 1);
-        ptx::mbar_init(ptx::smem_u32(&ms.drain), 1);
-        ms.abort = 0;
-        ptx::mbar_init_fence();
-    }
-    if (tid == 32) {
-        ptx::tma_prefetch_desc(&tmk);
-        ptx::tma_prefetch_desc(&tmv);
-    }
-    {   // Q: 48 rows x 256 B in two 64-column halves, 128-byte swizzle; rows beyond n_rows are zero
-        const uint4* q4 = reinterpret_cast<const uint4*>(a.q);
-        for (int i = tid; i < kMaxM * 16; i += kThreads) {
-            const int m = i >> 4, c = i & 15;
-            const uint4 val = (m < M) ? __ldg(q4 + m * 16 + c) : make_uint4(0u, 0u, 0u, 0u);
-            const int cc = c & 7;
-            const uint32_t off = kOffQ + (uint32_t)(c >> 3) * kQHalf + (uint32_t)(m >> 3) * 1024u +
-                                 (uint32_t)(m & 7) * 128u + ((uint32_t)(cc ^ (m & 7)) << 4);
-            *reinterpret_cast<uint4*>(base + off) = val;
-        }
-    }
-    ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = ms.tmem_base;
     volatile int* abort_flag = &ms.abort;
-    auto bar = [](const uint64_t& b) { return ptx::smem_u32(&b); };
+    if (tid == 0) {
+        VA_TRACE_AT(1);
+#ifdef VA_TRACE
+        if (g_trace) g_trace[(size_t)blockIdx.x * 256 + 3] = (unsigned long long)ntiles;
+#endif
+    }
     auto fail = [&]() {
         *abort_flag = 1;
         if (a.dev_status) atomicOr(a.dev_status, VA_DEV_TIMEOUT);
     };
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+    if (ntiles == 0) {
+        // empty split (or unusable positions): o = 0, lse = -inf
+        for (int i = tid; i < M * kD; i += kThreads) part_o[i] = 0.0f;
+        for (int i = tid; i < M; i += kThreads) part_lse[i] = -INFINITY;
+    } else if (warp == 0) {
+        // ------------------------------------------------------------ K producer
         if (lane == 0) {
-            int k_issued = 0, v_issued = 0;
-            for (int j = 0; j < ntiles; ++j) {
-                const long long t = P.t0 + 2LL * j;
-                const int halves = (t + 1 < P.t1) ? 2 : 1;
-                const int ks = j % kNK;
-                if (!ptx::mbar_wait(bar(ms.k_empty[ks]), ((j / kNK) & 1) ^ 1, abort_flag, kWaitNs)) {
+            if (kPrefetch > 0)
+                for (int j = k_first; j < min(kNK + kPrefetch, ntiles); ++j) prefetch_tile(&tmk, &tmk2, j);
+            int issued = k_first;
+            for (int j = k_first; j < ntiles; ++j) {
+                if (j < kNK) stagger(j);
+                if (!ptx::mbar_wait(bar(ms.k_empty[j % kNK]), ((j / kNK) & 1) ^ 1, abort_flag, kWaitNs)) {
                     fail();
                     break;
                 }
-                ptx::mbar_arrive_expect_tx(bar(ms.k_full[ks]), (uint32_t)halves * 2u * kHalfBox);
-                for (int hh = 0; hh < halves; ++hh) {
-                    const int slot = (int)(((t + hh) * kTile) % a.slots);
-                    for (int h = 0; h < 2; ++h)
-                        ptx::tma_load_2d(base_s + kOffK + ks * kStage + h * kDHalf + hh * kHalfBox, &tmk, h * 64, slot,
-                                         bar(ms.k_full[ks]));
-                }
-                k_issued = j + 1;
-                const int vs = j % kNV;
-                if (!ptx::mbar_wait(bar(ms.v_empty[vs]), ((j / kNV) & 1) ^ 1, abort_flag, kWaitNs)) {
-                    fail();
-                    break;
-                }
-                ptx::mbar_arrive_expect_tx(bar(ms.v_full[vs]), (uint32_t)halves * 2u * kHalfBox);
-                for (int hh = 0; hh < halves; ++hh) {
-                    const int slot = (int)(((t + hh) * kTile) % a.slots);
-                    for (int h = 0; h < 2; ++h)
-                        ptx::tma_load_2d(base_s + kOffV + vs * kStage + h * kDHalf + hh * kHalfBox, &tmv, h * 64, slot,
-                                         bar(ms.v_full[vs]));
-                }
-                v_issued = j + 1;
+                load_k(j);
+                issued = j + 1;
             }
-            // every issued copy has landed before this CTA may exit
-            for (int j = max(0, k_issued - kNK); j < k_issued; ++j)
+            for (int j = max(0, issued - kNK); j < issued; ++j)   // every issued copy lands before exit
                 ptx::mbar_wait(bar(ms.k_full[j % kNK]), (j / kNK) & 1, nullptr, kWaitNs);
-            for (int j = max(0, v_issued - kNV); j < v_issued; ++j)
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ V producer
+        if (lane == 0) {
+            if (kPrefetch > 0)
+                for (int j = v_first; j < min(kNV + kPrefetch, ntiles); ++j) prefetch_tile(&tmv, &tmv2, j);
+            int issued = v_first;
+            for (int j = v_first; j < ntiles; ++j) {
+                if (j < kNV) stagger(j);
+                if (!ptx::mbar_wait(bar(ms.v_empty[j % kNV]), ((j / kNV) & 1) ^ 1, abort_flag, kWaitNs)) {
+                    fail();
+                    break;
+                }
+                load_v(j);
+                issued = j + 1;
+            }
+            for (int j = max(0, issued - kNV); j < issued; ++j)
                 ptx::mbar_wait(bar(ms.v_full[j % kNV]), (j / kNV) & 1, nullptr, kWaitNs);
         }
+        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, 48, 0, 0);   // A = K, B = Q: both K-major
             constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, 48, 1, 1);   // A = V^T, B = P^T: MN-major
-            bool ok = true;
+            bool ok = ptx::mbar_wait(bar(ms.q_full), 0, abort_flag, kWaitNs);
             for (int j = 0; j <= ntiles && ok; ++j) {
                 if (j < ntiles) {
                     const int ks = j % kNK, sb = j & 1;
                     ok = ptx::mbar_wait(bar(ms.k_full[ks]), (j / kNK) & 1, abort_flag, kWaitNs) &&
                          ptx::mbar_wait(bar(ms.s_free[sb]), ((j >> 1) & 1) ^ 1, abort_flag, kWaitNs);
                     if (!ok) break;
+                    VA_TRACE_TILE(j, 2);
                     ptx::tc_fence_after();
                     const uint32_t d = tmem + (sb ? kColS1 : kColS0);
 #pragma unroll
@@ -257,25 +381,29 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk, const 
                                       ptx::smem_desc(base_s + kOffQ + h * kQHalf + off, 0, 1024), idesc_qk, kk > 0);
                     }
                     ptx::mma_commit(bar(ms.s_full[sb]));
-                    ptx::mma_commit(bar(ms.k_empty[ks]));
                 }
                 if (j >= 1) {
-                    const int i = j - 1, vs = i % kNV;
-                    ok = ptx::mbar_wait(bar(ms.v_full[vs]), (i / kNV) & 1, abort_flag, kWaitNs) &&
-                         ptx::mbar_wait(bar(ms.p_full), i & 1, abort_flag, kWaitNs);
+                    const int i = j - 1, vs = i % kNV, ps = i % kNK;
+                    ok = ptx::mbar_wait(bar(ms.v_full[vs]), (i / kNV) & 1, abort_flag, kWaitNs);
+                    VA_TRACE_TILE(i, 3);
+                    ok = ok && ptx::mbar_wait(bar(ms.p_full[i & 1]), (i >> 1) & 1, abort_flag, kWaitNs);
+                    VA_TRACE_TILE(i, 6);
                     if (!ok) break;
                     ptx::tc_fence_after();
-                    const long long t = P.t0 + 2LL * i;
+                    const long long t = tile_t(i);
                     const int nk = (t + 1 < P.t1) ? 8 : 4;
                     for (int kk = 0; kk < nk; ++kk) {
                         const uint64_t adesc = ptx::smem_desc(base_s + kOffV + vs * kStage + kk * 2048, kDHalf, 1024);
-                        ptx::mma_bf16(tmem + kColO, adesc, ptx::smem_desc(base_s + kOffPhi + kk * 2048, 8192, 1024),
-                                      idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
-                        ptx::mma_bf16(tmem + kColO, adesc, ptx::smem_desc(base_s + kOffPlo + kk * 2048, 8192, 1024),
-                                      idesc_pv, 1u);
+                        const uint32_t pbase = base_s + kOffK + ps * kStage + kk * 2048;
+                        ptx::mma_bf16(tmem + kColO, adesc, ptx::smem_desc(pbase + kPhiInStage, 8192, 1024), idesc_pv,
+                                      (i > 0 || kk > 0) ? 1u : 0u);
+                        ptx::mma_bf16(tmem + kColO, adesc, ptx::smem_desc(pbase + kPloInStage, 8192, 1024), idesc_pv,
+                                      1u);
                     }
                     ptx::mma_commit(bar(ms.pv_done));
                     ptx::mma_commit(bar(ms.v_empty[vs]));
+                    ptx::mma_commit(bar(ms.k_empty[ps]));
+                    if (i == ntiles - 1) ptx::mma_commit(bar(ms.o_ready));   // the accumulator is final
                 }
             }
             if (!ok) fail();
@@ -285,8 +413,10 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk, const 
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax / accumulator warps
+        const int sw = warp - kSoftWarp0;     // 0..7
         const int q = warp & 3;               // TMEM lane quadrant this warp may access
-        const int wq = warp - 2;
+        const int ch = sw >> 2;               // column half: matrix rows [24 ch, 24 ch + 24)
+        const int n0 = ch * kCols;
         const int L = q * 32 + lane;          // key of the tile (S^T) and output column d (O^T)
         const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
         const float c = a.scale * 1.4426950408889634f;   // scores in log2 units
@@ -295,155 +425,164 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk, const 
             all_lo = max(all_lo, ms.row_lo[r]);
             all_hi = min(all_hi, ms.row_hi[r]);
         }
-        float ref[kMaxM], l[kMaxM];
+        float ref[kCols], l[kCols];
 #pragma unroll
-        for (int n = 0; n < kMaxM; ++n) {
-            ref[n] = kRefInit;
-            l[n] = 0.0f;
+        for (int i = 0; i < kCols; ++i) {
+            ref[i] = ms.ref[n0 + i];
+            l[i] = 0.0f;
         }
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
-            const long long t = P.t0 + 2LL * j;
+            const long long t = tile_t(j);
             const int nkeys = (t + 1 < P.t1) ? 128 : 64;
             const long long kbase = t * kTile;
             const long long kp = kbase + L;
             const int sb = j & 1;
             if (!ptx::mbar_wait(bar(ms.s_full[sb]), (j >> 1) & 1, abort_flag, kWaitNs)) ok = false;
+            if (sw == 0 && lane == 0) VA_TRACE_TILE(j, 4);
             ptx::tc_fence_after();
-            float x[kMaxM];
-            ptx::tmem_ld48_wait(tl + (sb ? kColS1 : kColS0), x);
+            float x[kCols];
+            ptx::tmem_ld24_wait(tl + (sb ? kColS1 : kColS0) + n0, x);
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(ms.s_free[sb]));
 
-            // masked scores in log2 units
-            if (kbase >= all_lo && kbase + nkeys <= all_hi) {
-                // every live row sees every key of the tile; lanes past a half tile hold stale rows
-                const bool key_in = L < nkeys;
+            // visibility: interior tiles need only the half-tile check; padding rows have ref = +inf
+            const bool interior = kbase >= all_lo && kbase + nkeys <= all_hi;
+            bool vis[kCols];
+            {   // this column half holds verify rows 4 ch .. 4 ch + 3
+                bool rv[kMaxRows / 2];
 #pragma unroll
-                for (int n = 0; n < kMaxM; ++n) x[n] = (key_in && n < ML) ? x[n] * c : -INFINITY;
-            } else {
-                bool vis[kMaxRows];
-#pragma unroll
-                for (int r = 0; r < kMaxRows; ++r) vis[r] = (r < a.n_live) && kp >= ms.row_lo[r] && kp < ms.row_hi[r];
-#pragma unroll
-                for (int n = 0; n < kMaxM; ++n) x[n] = vis[n / kH] ? x[n] * c : -INFINITY;
-            }
-            // raise the reference maxima only when a score exceeds them by more than 2^kThresh
-            float umax = -INFINITY;
-#pragma unroll
-            for (int n = 0; n < kMaxM; ++n) umax = fmaxf(umax, x[n] - ref[n]);
-            const unsigned want = __any_sync(0xffffffffu, umax > kThresh);
-            if (lane == 0) ms.vote[j & 1][wq] = want ? 1 : 0;
-            ptx::named_bar_sync(1, 128);
-            const bool rescale = (ms.vote[j & 1][0] | ms.vote[j & 1][1] | ms.vote[j & 1][2] | ms.vote[j & 1][3]) != 0;
-            // PV(j-1) done: the P buffers may be rewritten and the accumulator is stable
-            if (j > 0 && !ptx::mbar_wait(bar(ms.pv_done), (j - 1) & 1, abort_flag, kWaitNs)) ok = false;
-            if (rescale) {
-                float v[kMaxM];
-#pragma unroll
-                for (int n = 0; n < kMaxM; ++n) v[n] = x[n];
-                warp_reduce_scatter48<true>(v, lane);
-                const int cb = scatter_col_base(lane);
-                if ((lane & 1) == 0) {
-                    ms.red[wq][cb] = v[0];
-                    ms.red[wq][cb + 1] = v[1];
-                    ms.red[wq][cb + 2] = v[2];
+                for (int k = 0; k < kMaxRows / 2; ++k) {
+                    const int r = (kMaxRows / 2) * ch + k;
+                    rv[k] = interior ? (L < nkeys) : ((r < a.n_live) && kp >= ms.row_lo[r] && kp < ms.row_hi[r]);
                 }
-                ptx::named_bar_sync(1, 128);
-                if (L < kMaxM) {
+#pragma unroll
+                for (int i = 0; i < kCols; ++i) vis[i] = rv[i / kH];
+            }
+            float p[kCols];
+            float pmax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < kCols; ++i) {
+                p[i] = vis[i] ? ptx::ex2(fmaf(x[i], c, -ref[i])) : 0.0f;
+                pmax = fmaxf(pmax, p[i]);
+            }
+            // raise the reference maxima only when a probability exceeds 2^8 (CTA-wide vote)
+            const unsigned want = __any_sync(0xffffffffu, !(pmax <= kThresh));
+            if (lane == 0) ms.vote[j & 1][sw] = want ? 1 : 0;
+            ptx::named_bar_sync(1, kSoftThreads);
+            int any = 0;
+#pragma unroll
+            for (int w = 0; w < kSoftWarps; ++w) any |= ms.vote[j & 1][w];
+            if (any) {
+                // PV(j-1) must be done before the accumulator is rescaled.  (s_full(j) was committed after
+                // PV(j-2), so pv_done can be at most one phase behind here.)
+                if (j > 0 && !ptx::mbar_wait(bar(ms.pv_done), (j - 1) & 1, abort_flag, kWaitNs)) ok = false;
+                float v[kCols];
+#pragma unroll
+                for (int i = 0; i < kCols; ++i) v[i] = vis[i] ? x[i] * c : -INFINITY;
+                warp_reduce_scatter24<true>(v, lane);
+                const int cb = n0 + scatter_col_base(lane);
+                if ((lane & 3) == 0) {
+                    ms.red[q][cb] = v[0];
+                    ms.red[q][cb + 1] = v[1];
+                    ms.red[q][cb + 2] = v[2];
+                }
+                ptx::named_bar_sync(1, kSoftThreads);
+                if (ch == 0 && L < kMaxM) {
                     const float cm = fmaxf(fmaxf(ms.red[0][L], ms.red[1][L]), fmaxf(ms.red[2][L], ms.red[3][L]));
                     const float old = ms.ref[L];
                     const float nw = fmaxf(old, cm);
-                    ms.alpha[L] = ptx::ex2(old - nw);
+                    ms.alpha[L] = (nw == old) ? 1.0f : ptx::ex2(old - nw);
                     ms.ref[L] = nw;
                 }
-                ptx::named_bar_sync(1, 128);
+                ptx::named_bar_sync(1, kSoftThreads);
 #pragma unroll
-                for (int n = 0; n < kMaxM; ++n) {
-                    ref[n] = ms.ref[n];
-                    l[n] *= ms.alpha[n];
+                for (int i = 0; i < kCols; ++i) {
+                    ref[i] = ms.ref[n0 + i];
+                    l[i] *= ms.alpha[n0 + i];
+                    p[i] = vis[i] ? ptx::ex2(fmaf(x[i], c, -ref[i])) : 0.0f;
                 }
                 if (j > 0) {
                     ptx::tc_fence_after();
+                    float o[kCols];
+                    ptx::tmem_ld24_wait(tl + kColO + n0, o);
 #pragma unroll
-                    for (int c16 = 0; c16 < 3; ++c16) {
-                        float o[16];
-                        ptx::tmem_ld16_wait(tl + kColO + 16 * c16, o);
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) o[i] *= ms.alpha[16 * c16 + i];
-                        ptx::tmem_st16(tl + kColO + 16 * c16, o);
-                    }
+                    for (int i = 0; i < kCols; ++i) o[i] *= ms.alpha[n0 + i];
+                    ptx::tmem_st16(tl + kColO + n0, o);
+                    ptx::tmem_st8(tl + kColO + n0 + 16, o + 16);
                     ptx::tmem_wait_st();
                 }
             }
-            // probabilities; hi/lo bf16 split for the PV product
-            uint32_t hi_w[kMaxM / 2], lo_w[kMaxM / 2];
+            // running sums; hi/lo bf16 split of P for the PV product
+            uint32_t hi_w[kCols / 2], lo_w[kCols / 2];
 #pragma unroll
-            for (int i = 0; i < kMaxM / 2; ++i) {
-                const float p0 = ptx::ex2(x[2 * i] - ref[2 * i]);
-                const float p1 = ptx::ex2(x[2 * i + 1] - ref[2 * i + 1]);
+            for (int i = 0; i < kCols / 2; ++i) {
+                const float p0 = p[2 * i], p1 = p[2 * i + 1];
                 l[2 * i] += p0;
                 l[2 * i + 1] += p1;
                 const uint32_t hb = pack_bf16x2(p0, p1);
                 hi_w[i] = hb;
                 lo_w[i] = pack_bf16x2(p0 - __uint_as_float(hb << 16), p1 - __uint_as_float(hb & 0xFFFF0000u));
             }
-            // V rows of positions this split does not own are zeroed before PV reads them
+            // V rows of positions this split does not own are zeroed before PV reads them (column half ch)
             const int vs = j % kNV;
             if (kbase < own_lo || kbase + nkeys > own_hi) {
                 if (!ptx::mbar_wait(bar(ms.v_full[vs]), (j / kNV) & 1, abort_flag, kWaitNs)) ok = false;
                 if (L < nkeys && (kp < own_lo || kp >= own_hi)) {
-                    for (int h = 0; h < 2; ++h) {
-                        uint4* row = reinterpret_cast<uint4*>(base + kOffV + vs * kStage + h * kDHalf +
-                                                              (uint32_t)(L >> 3) * 1024u + (uint32_t)(L & 7) * 128u);
+                    uint4* row = reinterpret_cast<uint4*>(base + kOffV + vs * kStage + ch * kDHalf +
+                                                          (uint32_t)(L >> 3) * 1024u + (uint32_t)(L & 7) * 128u);
 #pragma unroll
-                        for (int cc = 0; cc < 8; ++cc) row[cc] = make_uint4(0u, 0u, 0u, 0u);
-                    }
+                    for (int cc = 0; cc < 8; ++cc) row[cc] = make_uint4(0u, 0u, 0u, 0u);
                 }
             }
-            // row L of P^T (keys x 48 matrix rows), 128-byte swizzle
+            // row L of P^T (keys x 48 matrix rows), columns [n0, n0 + 24): 16-byte chunks 3 ch .. 3 ch + 2,
+            // written over K of this tile (QK(j) has completed: S^T(j) was read above)
             {
-                const uint32_t roff = (uint32_t)(L >> 3) * 1024u + (uint32_t)(L & 7) * 128u;
+                const uint32_t roff = kOffK + (uint32_t)(j % kNK) * kStage + (uint32_t)(L >> 3) * 1024u + (uint32_t)(L & 7) * 128u;
 #pragma unroll
-                for (int cc = 0; cc < 6; ++cc) {
-                    const uint32_t off = roff + ((uint32_t)(cc ^ (L & 7)) << 4);
-                    *reinterpret_cast<uint4*>(base + kOffPhi + off) =
-                        make_uint4(hi_w[4 * cc], hi_w[4 * cc + 1], hi_w[4 * cc + 2], hi_w[4 * cc + 3]);
-                    *reinterpret_cast<uint4*>(base + kOffPlo + off) =
-                        make_uint4(lo_w[4 * cc], lo_w[4 * cc + 1], lo_w[4 * cc + 2], lo_w[4 * cc + 3]);
+                for (int k = 0; k < 3; ++k) {
+                    const uint32_t off = roff + ((uint32_t)((3 * ch + k) ^ (L & 7)) << 4);
+                    *reinterpret_cast<uint4*>(base + kPhiInStage + off) =
+                        make_uint4(hi_w[4 * k], hi_w[4 * k + 1], hi_w[4 * k + 2], hi_w[4 * k + 3]);
+                    *reinterpret_cast<uint4*>(base + kPloInStage + off) =
+                        make_uint4(lo_w[4 * k], lo_w[4 * k + 1], lo_w[4 * k + 2], lo_w[4 * k + 3]);
                 }
             }
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(ms.p_full));
+            if (lane == 0) ptx::mbar_arrive(bar(ms.p_full[j & 1]));
+            if (sw == 0 && lane == 0) VA_TRACE_TILE(j, 5);
         }
         // ------------------------------------------------------------ epilogue
-        if (!ptx::mbar_wait(bar(ms.pv_done), (ntiles - 1) & 1, abort_flag, kWaitNs)) ok = false;
-        ptx::tc_fence_after();
-        float o[kMaxM];
-        ptx::tmem_ld48_wait(tl + kColO, o);
-        warp_reduce_scatter48<false>(l, lane);
+        // row sums first: they do not depend on the last PV, which is still running
+        warp_reduce_scatter24<false>(l, lane);
         {
-            const int cb = scatter_col_base(lane);
-            if ((lane & 1) == 0) {
-                ms.red[wq][cb] = l[0];
-                ms.red[wq][cb + 1] = l[1];
-                ms.red[wq][cb + 2] = l[2];
+            const int cb = n0 + scatter_col_base(lane);
+            if ((lane & 3) == 0) {
+                ms.red[q][cb] = l[0];
+                ms.red[q][cb + 1] = l[1];
+                ms.red[q][cb + 2] = l[2];
             }
         }
-        ptx::named_bar_sync(1, 128);
-        if (L < kMaxM) ms.alpha[L] = (ms.red[0][L] + ms.red[1][L]) + (ms.red[2][L] + ms.red[3][L]);
-        ptx::named_bar_sync(1, 128);
+        ptx::named_bar_sync(1, kSoftThreads);
+        if (ch == 0 && L < kMaxM) {
+            const float lt = (ms.red[0][L] + ms.red[1][L]) + (ms.red[2][L] + ms.red[3][L]);
+            ms.alpha[L] = lt;
+            ms.inv_l[L] = lt > 0.0f ? 1.0f / lt : 0.0f;
+        }
+        ptx::named_bar_sync(1, kSoftThreads);
+        if (!ptx::mbar_wait(bar(ms.o_ready), 0, abort_flag, kWaitNs)) ok = false;
+        ptx::tc_fence_after();
+        float o[kCols];
+        ptx::tmem_ld24_wait(tl + kColO + n0, o);
 #pragma unroll
-        for (int n = 0; n < kMaxM; ++n) {
-            if (n < M) {
-                const float lt = ms.alpha[n];
-                part_o[n * kD + L] = lt > 0.0f ? o[n] / lt : 0.0f;
-            }
+        for (int i = 0; i < kCols; ++i) {
+            const int n = n0 + i;
+            if (n < M) part_o[n * kD + L] = o[i] * ms.inv_l[n];
         }
-        if (L < M) {
+        if (ch == 0 && L < M) {
             const float lt = ms.alpha[L];
             part_lse[L] = lt > 0.0f ? (ms.ref[L] + log2f(lt)) * 0.6931471805599453f : -INFINITY;
         }
@@ -453,6 +592,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk, const 
     // ---------------------------------------------------------------- teardown
     ptx::tc_fence_before();
     __syncthreads();
+    if (tid == 0) VA_TRACE_AT(2);
     if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
@@ -480,14 +620,14 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [slots][128] bf16 rows, boxes of 64 rows x 64 columns with the 128-byte swizzle; rows past the
-// end read as zero.
-bool encode_kv_map(CUtensorMap* map, const void* base, int slots) {
+// [rows][128] bf16, boxes of box_rows rows x 64 columns with the 128-byte swizzle; rows past the end
+// read as zero.
+bool encode_rows_map(CUtensorMap* map, const void* base, int rows, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)slots};
+    const cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
-    const cuuint32_t box[2] = {64, 64};
+    const cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
     const cuuint32_t elem[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -497,12 +637,27 @@ bool encode_kv_map(CUtensorMap* map, const void* base, int slots) {
 }  // namespace tc
 
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
-    CUtensorMap tmk, tmv;
-    if (!tc::encode_kv_map(&tmk, a.k, a.slots) || !tc::encode_kv_map(&tmv, a.v, a.slots)) return cudaErrorInvalidValue;
+    CUtensorMap tmq, tmk, tmv, tmk2, tmv2;
+    if (!tc::encode_rows_map(&tmq, a.q, a.n_rows * kH, 48) || !tc::encode_rows_map(&tmk, a.k, a.slots, 64) ||
+        !tc::encode_rows_map(&tmv, a.v, a.slots, 64) || !tc::encode_rows_map(&tmk2, a.k, a.slots, 128) ||
+        !tc::encode_rows_map(&tmv2, a.v, a.slots, 128))
+        return cudaErrorInvalidValue;
     cudaError_t e = ensure_smem_attr((const void*)tc::attn_tc_kernel, (int)tc::kSmemBytes);
     if (e != cudaSuccess) return e;
-    tc::attn_tc_kernel<<<a.n_splits, tc::kThreads, tc::kSmemBytes, stream>>>(a, tmk, tmv);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    pdl_config(&cfg, attr, dim3(a.n_splits), dim3(tc::kThreads), tc::kSmemBytes, stream);
+    e = cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel, a, tmq, tmk, tmv, tmk2, tmv2);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace va
+
+#ifdef VA_TRACE
+// Debug build only: point the split kernel's timeline probe at a device buffer of n_splits x 256
+// unsigned 64-bit words (NULL turns it off).
+extern "C" VA_API int va_debug_set_trace(void* device_buffer) {
+    unsigned long long* p = static_cast<unsigned long long*>(device_buffer);
+    return cudaMemcpyToSymbol(va::tc::g_trace, &p, sizeof p) == cudaSuccess ? VA_OK : VA_CUDA_ERROR;
+}
+#endif

@@ -5,13 +5,18 @@
 // BF16 rounding boundary (the output is rounded to bf16 once, here).
 #include <cuda_bf16.h>
 
+#include "tc_ptx.cuh"
 #include "va_internal.cuh"
 
 namespace va {
 
-constexpr int kCombineThreads = kD;   // one thread per output column d
+constexpr int kCombineWarps = 8;
+constexpr int kCombineThreads = 32 * kCombineWarps;
 
-// One CTA per matrix row m = r * 6 + h.  Shared memory holds the split weights exp(lse_s - L).
+// One CTA per matrix row m = r * 6 + h.  Warp w accumulates the splits s = w, w + 8, ...: each lane owns
+// four output columns and keeps four independent accumulators (one per unrolled split), with the four
+// splits' loads issued before any of them is used.  The eight warp totals are then added in a fixed
+// order.  Shared memory holds the split weights exp(lse_s - L).
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* __restrict__ part_o,
                                                                   const float* __restrict__ part_lse,
                                                                   int n_splits, const float* __restrict__ sink,
@@ -19,80 +24,102 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* _
                                                                   __nv_bfloat16* __restrict__ out,
                                                                   float* __restrict__ out_lse) {
     extern __shared__ float w[];          // [n_splits]
-    __shared__ float red[kCombineThreads / 32];
-    __shared__ float s_L;
+    __shared__ float red[kCombineWarps];
+    __shared__ float4 part[kCombineWarps][kD / 4];
+    __shared__ float s_mx, s_L;
     const int m = blockIdx.x;
     const int r = m / kH, h = m - r * kH;
-    const int d = threadIdx.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int M = n_rows * kH;
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();   // every global access comes after this
     if (r >= n_live) {
-        out[(long long)m * kD + d] = __float2bfloat16_rn(0.0f);
-        if (out_lse && d == 0) out_lse[m] = -INFINITY;
+        if (tid < kD) out[(long long)m * kD + tid] = __float2bfloat16_rn(0.0f);
+        if (out_lse && tid == 0) out_lse[m] = -INFINITY;
         return;
     }
-    const float sk = sink ? __ldg(sink + h) : -INFINITY;
+    const float sk = sink ? __ldcg(sink + h) : -INFINITY;
 
     // L = logsumexp({lse_s} U {sink})
     float mx = sk;
-    for (int s = d; s < n_splits; s += kCombineThreads) {
-        const float l = __ldg(part_lse + (long long)s * M + m);
+    for (int s = tid; s < n_splits; s += kCombineThreads) {
+        const float l = __ldcg(part_lse + (long long)s * M + m);
         w[s] = l;
         mx = fmaxf(mx, l);
     }
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if ((d & 31) == 0) red[d >> 5] = mx;
+    if (lane == 0) red[warp] = mx;
     __syncthreads();
-    mx = red[0];
-    for (int i = 1; i < kCombineThreads / 32; ++i) mx = fmaxf(mx, red[i]);
+    if (tid == 0) {
+        float t = red[0];
+        for (int i = 1; i < kCombineWarps; ++i) t = fmaxf(t, red[i]);
+        s_mx = t;
+    }
     __syncthreads();
+    mx = s_mx;
     if (mx == -INFINITY) {  // nothing visible and no sink
-        out[(long long)m * kD + d] = __float2bfloat16_rn(0.0f);
-        if (out_lse && d == 0) out_lse[m] = -INFINITY;
+        if (tid < kD) out[(long long)m * kD + tid] = __float2bfloat16_rn(0.0f);
+        if (out_lse && tid == 0) out_lse[m] = -INFINITY;
         return;
     }
-    float z = (d == 0) ? expf(sk - mx) : 0.0f;
-    for (int s = d; s < n_splits; s += kCombineThreads) z += expf(w[s] - mx);
+    float z = (tid == 0) ? expf(sk - mx) : 0.0f;
+    for (int s = tid; s < n_splits; s += kCombineThreads) z += expf(w[s] - mx);
     for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-    if ((d & 31) == 0) red[d >> 5] = z;
+    if (lane == 0) red[warp] = z;
     __syncthreads();
-    if (d == 0) {
+    if (tid == 0) {
         float zt = 0.0f;
-        for (int i = 0; i < kCombineThreads / 32; ++i) zt += red[i];
+        for (int i = 0; i < kCombineWarps; ++i) zt += red[i];
         s_L = mx + logf(zt);
     }
     __syncthreads();
     const float L = s_L;
-    for (int s = d; s < n_splits; s += kCombineThreads) w[s] = expf(w[s] - L);
+    for (int s = tid; s < n_splits; s += kCombineThreads) w[s] = expf(w[s] - L);
     __syncthreads();
 
-    // out[d] = sum_s w_s * o_s[d]: four independent chains, loads issued together
-    const float* po = part_o + (long long)m * kD + d;
-    const long long stride = (long long)M * kD;
-    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-    int s = 0;
-    for (; s + 4 <= n_splits; s += 4) {
-        const float o0 = __ldg(po + (s + 0) * stride);
-        const float o1 = __ldg(po + (s + 1) * stride);
-        const float o2 = __ldg(po + (s + 2) * stride);
-        const float o3 = __ldg(po + (s + 3) * stride);
-        acc0 = fmaf(w[s + 0], o0, acc0);
-        acc1 = fmaf(w[s + 1], o1, acc1);
-        acc2 = fmaf(w[s + 2], o2, acc2);
-        acc3 = fmaf(w[s + 3], o3, acc3);
+    // out[d] = sum_s w_s o_s[d]
+    const float4* po = reinterpret_cast<const float4*>(part_o + (long long)m * kD) + lane;
+    const long long stride4 = (long long)M * kD / 4;
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
+    int s = warp;
+    for (; s + 3 * kCombineWarps < n_splits; s += 4 * kCombineWarps) {
+        const float4 o0 = __ldcg(po + (long long)(s + 0 * kCombineWarps) * stride4);
+        const float4 o1 = __ldcg(po + (long long)(s + 1 * kCombineWarps) * stride4);
+        const float4 o2 = __ldcg(po + (long long)(s + 2 * kCombineWarps) * stride4);
+        const float4 o3 = __ldcg(po + (long long)(s + 3 * kCombineWarps) * stride4);
+        const float w0 = w[s], w1 = w[s + kCombineWarps], w2 = w[s + 2 * kCombineWarps], w3 = w[s + 3 * kCombineWarps];
+        a0.x = fmaf(w0, o0.x, a0.x); a0.y = fmaf(w0, o0.y, a0.y); a0.z = fmaf(w0, o0.z, a0.z); a0.w = fmaf(w0, o0.w, a0.w);
+        a1.x = fmaf(w1, o1.x, a1.x); a1.y = fmaf(w1, o1.y, a1.y); a1.z = fmaf(w1, o1.z, a1.z); a1.w = fmaf(w1, o1.w, a1.w);
+        a2.x = fmaf(w2, o2.x, a2.x); a2.y = fmaf(w2, o2.y, a2.y); a2.z = fmaf(w2, o2.z, a2.z); a2.w = fmaf(w2, o2.w, a2.w);
+        a3.x = fmaf(w3, o3.x, a3.x); a3.y = fmaf(w3, o3.y, a3.y); a3.z = fmaf(w3, o3.z, a3.z); a3.w = fmaf(w3, o3.w, a3.w);
     }
-    if (s + 0 < n_splits) acc0 = fmaf(w[s + 0], __ldg(po + (s + 0) * stride), acc0);
-    if (s + 1 < n_splits) acc1 = fmaf(w[s + 1], __ldg(po + (s + 1) * stride), acc1);
-    if (s + 2 < n_splits) acc2 = fmaf(w[s + 2], __ldg(po + (s + 2) * stride), acc2);
-    out[(long long)m * kD + d] = __float2bfloat16_rn((acc0 + acc1) + (acc2 + acc3));
-    if (out_lse && d == 0) out_lse[m] = L;
+    for (; s < n_splits; s += kCombineWarps) {
+        const float4 o0 = __ldcg(po + (long long)s * stride4);
+        const float w0 = w[s];
+        a0.x = fmaf(w0, o0.x, a0.x); a0.y = fmaf(w0, o0.y, a0.y); a0.z = fmaf(w0, o0.z, a0.z); a0.w = fmaf(w0, o0.w, a0.w);
+    }
+    part[warp][lane] = make_float4((a0.x + a1.x) + (a2.x + a3.x), (a0.y + a1.y) + (a2.y + a3.y),
+                                   (a0.z + a1.z) + (a2.z + a3.z), (a0.w + a1.w) + (a2.w + a3.w));
+    __syncthreads();
+    if (tid < kD) {
+        const float* pf = reinterpret_cast<const float*>(part);
+        float acc = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kCombineWarps; ++i) acc += pf[i * kD + tid];
+        out[(long long)m * kD + tid] = __float2bfloat16_rn(acc);
+        if (out_lse && tid == 0) out_lse[m] = L;
+    }
 }
 
 cudaError_t launch_combine(const float* part_o, const float* part_lse, int n_splits, const float* sink,
                            int n_rows, int n_live, uint16_t* out, float* out_lse, cudaStream_t stream) {
     const size_t smem = sizeof(float) * (size_t)(n_splits > 0 ? n_splits : 1);
-    combine_kernel<<<n_rows * kH, kCombineThreads, smem, stream>>>(
-        part_o, part_lse, n_splits, sink, n_rows, n_live, reinterpret_cast<__nv_bfloat16*>(out), out_lse);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    pdl_config(&cfg, attr, dim3(n_rows * kH), dim3(kCombineThreads), smem, stream);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, combine_kernel, part_o, part_lse, n_splits, sink, n_rows, n_live,
+                                             reinterpret_cast<__nv_bfloat16*>(out), out_lse);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace va

@@ -36,17 +36,22 @@ struct Plan {
     int status;            // VA_DEV_* bits, 0 if the positions are usable
 };
 
+// Also returns the live rows' positions in row_pos[] (entries past n_live are 0).
 __device__ __forceinline__ Plan make_plan(const int32_t* __restrict__ pos, int n_live, int window,
-                                          int slots, int n_splits, int split) {
+                                          int slots, int n_splits, int split, int (&row_pos)[kMaxRows]) {
     Plan P;
     P.lo = P.hi = P.t0 = P.t1 = 0;
     P.status = 0;
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) row_pos[r] = (r < n_live) ? __ldcg(pos + r) : 0;
     if (n_live <= 0) return P;
-    const int p0 = __ldg(pos);
+    const int p0 = row_pos[0];
     int prev = p0, last = p0;
     if (p0 < 0) P.status |= VA_DEV_NEGATIVE_POS;
-    for (int r = 1; r < n_live; ++r) {
-        const int p = __ldg(pos + r);
+#pragma unroll
+    for (int r = 1; r < kMaxRows; ++r) {
+        if (r >= n_live) break;
+        const int p = row_pos[r];
         if (p < 0) P.status |= VA_DEV_NEGATIVE_POS;
         if (p < prev) P.status |= VA_DEV_NOT_MONOTONE;
         prev = p;
@@ -68,6 +73,20 @@ __device__ __forceinline__ Plan make_plan(const int32_t* __restrict__ pos, int n
 // Opt a kernel into `bytes` of dynamic shared memory on the current device, once per device
 // (so that a later launch under stream capture issues no attribute call).
 cudaError_t ensure_smem_attr(const void* kernel, int bytes);
+
+// Launch configuration with programmatic stream serialisation: the kernel may start while the previous
+// kernel of the stream finishes; it waits for it (griddepcontrol.wait) before touching memory.
+inline void pdl_config(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream) {
+    cfg->gridDim = grid;
+    cfg->blockDim = block;
+    cfg->dynamicSmemBytes = smem;
+    cfg->stream = stream;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
+}
 
 // Launchers (return the cudaError_t of the launch).
 cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, int n_live, uint16_t* k_cache,

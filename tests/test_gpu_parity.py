@@ -19,6 +19,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _assert_parity(got, ref, w, check_partials=True):
+    assert got["status"] == 0, f"device status {got['status']:#x}"
     m = parity.out_metrics(got["out"], ref["out_bf16"], w.n_live)
     assert parity.out_ok(m), m
     assert parity.lse_err(got["out_lse"][:w.n_live], ref["lse"][:w.n_live]) <= parity.LSE_ABS

@@ -16,7 +16,7 @@ import threading
 
 __all__ = [
     "VerifyAttnError", "lib", "lib_path", "kv_ring_append", "verify_attn_full", "verify_attn_swa",
-    "attn_split_combine", "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string",
+    "attn_split_combine", "verify_attn_full_noalloc", "NOALLOC_MAX_SPLITS", "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string",
     "HEAD_DIM", "Q_HEADS", "MAX_ROWS", "TILE", "MAX_SPLITS", "EXPORTS",
     "VA_OK", "VA_INVALID_ARG", "VA_UNSUPPORTED", "VA_RING_TOO_SMALL", "VA_CUDA_ERROR",
 ]
@@ -24,7 +24,9 @@ __all__ = [
 HEAD_DIM, Q_HEADS, MAX_ROWS, TILE, MAX_SPLITS = 128, 6, 8, 64, 4096
 VA_OK, VA_INVALID_ARG, VA_UNSUPPORTED, VA_RING_TOO_SMALL, VA_CUDA_ERROR = 0, 1, 2, 3, 4
 EXPORTS = ("kv_ring_append", "verify_attn_full", "verify_attn_swa", "attn_split_combine",
-           "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string")
+           "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string",
+           "verify_attn_full_noalloc")
+NOALLOC_MAX_SPLITS = 160
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _lib = {}
@@ -55,7 +57,9 @@ def lib(variant: str = "") -> ctypes.CDLL:
         L.verify_attn_full.argtypes = [p, i, i, p, p, i, p, f, i, p, p, ctypes.POINTER(i), p, p]
         L.verify_attn_swa.argtypes = [p, i, i, p, p, i, i, p, f, i, p, p, ctypes.POINTER(i), p, p]
         L.attn_split_combine.argtypes = [p, p, i, p, i, i, p, p, p]
-        for fn in ("kv_ring_append", "verify_attn_full", "verify_attn_swa", "attn_split_combine"):
+        L.verify_attn_full_noalloc.argtypes = [p, i, i, p, p, i, p, f, i, p, p, p, ctypes.POINTER(i), p, p]
+        for fn in ("kv_ring_append", "verify_attn_full", "verify_attn_swa", "attn_split_combine",
+                   "verify_attn_full_noalloc"):
             getattr(L, fn).restype = i
         L.va_workspace_bytes.argtypes = [i]
         L.va_workspace_bytes.restype = ctypes.c_size_t
@@ -142,3 +146,16 @@ def attn_split_combine(part_o, part_lse, n_splits: int, sink, n_live: int, out, 
                                          int(out.shape[0]), int(n_live), _ptr(out), _ptr(out_lse),
                                          _stream(stream))
     _check("attn_split_combine", st)
+
+
+def verify_attn_full_noalloc(q, n_live: int, k_cache, v_cache, pos, scale: float, sink, out, out_lse=None,
+                             n_splits: int = 0, dev_status=None, stream=None, variant: str = "") -> int:
+    """Full-attention verify call plus combine with the partials in the library's own fixed device
+    buffer (for callers that cannot allocate); returns the split count launched."""
+    used = ctypes.c_int(0)
+    st = lib(variant).verify_attn_full_noalloc(_ptr(q), int(q.shape[0]), int(n_live), _ptr(k_cache), _ptr(v_cache),
+                                               int(k_cache.shape[0]), _ptr(pos), float(scale), int(n_splits),
+                                               _ptr(sink), _ptr(out), _ptr(out_lse), ctypes.byref(used),
+                                               _ptr(dev_status), _stream(stream))
+    _check("verify_attn_full_noalloc", st)
+    return used.value

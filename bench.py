@@ -159,6 +159,28 @@ class Clocks:
                 "reasons": sorted(reasons), "samples": len(busy)}
 
 
+KERNEL_SOURCES = ("speculative_decode_verify_gb300/csrc/attn_tc.cu", "speculative_decode_verify_gb300/csrc/tc_ptx.cuh",
+                  "speculative_decode_verify_gb300/csrc/va_internal.cuh")
+
+
+def measured_traffic():
+    """DRAM bytes per split-attention launch from the committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    import hashlib
+    import re
+    try:
+        txt = open(os.path.join(ROOT, "profiles", "attn_tc_192k.md")).read()
+        vals = dict(re.findall(r"^(traffic_bytes_per_launch|kernel_source_sha256)=(\S+)$", txt, re.M))
+        h = hashlib.sha256()
+        for f in KERNEL_SOURCES:
+            h.update(open(os.path.join(ROOT, f), "rb").read())
+        if vals.get("kernel_source_sha256") == h.hexdigest():
+            return int(vals["traffic_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
 def measured_peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -398,7 +420,7 @@ def ours(args, dist: Dist):
                    "parallelism": f"replicas x{dist.world} (one KV head per GPU, no collective)"},
         "us_per_call": t_max / args.steps / len(calls) * 1e6,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "kernel": "verify_attn_full split kernel",
+                     "traffic": measured_traffic(), "kernel": "verify_attn_full split kernel",
                      "us_per_launch": mean_attn * 1e6, "launches": len(attn_s),
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs" if peaks else "fallback 6.8 TB/s"},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -16,18 +16,20 @@ __global__ void __launch_bounds__(32) kv_append_kernel(const uint4* __restrict__
     const int lane = threadIdx.x;
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();   // every global access comes after this
+    constexpr int kChunks = kD * 2 / 16;   // 16 chunks of 16 B per row
+    const int c = lane & (kChunks - 1);
+    // the row and its position are loaded together (one memory round trip)
+    const uint4 val = lane < kChunks ? __ldcg(k_new + (long long)r * kChunks + c) : __ldcg(v_new + (long long)r * kChunks + c);
     const int p = __ldcg(pos + r);
     if (p < 0) {
         if (lane == 0 && dev_status) atomicOr(dev_status, VA_DEV_NEGATIVE_POS);
         return;
     }
     const long long slot = (long long)p % slots;
-    constexpr int kChunks = kD * 2 / 16;   // 16 chunks of 16 B per row
-    const int c = lane & (kChunks - 1);
     if (lane < kChunks)
-        k_cache[slot * kChunks + c] = __ldcg(k_new + (long long)r * kChunks + c);
+        k_cache[slot * kChunks + c] = val;
     else
-        v_cache[slot * kChunks + c] = __ldcg(v_new + (long long)r * kChunks + c);
+        v_cache[slot * kChunks + c] = val;
 }
 
 cudaError_t launch_append(const uint16_t* k_new, const uint16_t* v_new, int n_live, uint16_t* k_cache,

@@ -1,6 +1,6 @@
 // Log-sum-exp merge of the split partials with the learned sink folded in.
 // IQuestRT report, "Read only the KV tiles needed by the current positions": a separate combine
-// kernel issues the partial loads together and uses four independent FP32 accumulation chains;
+// kernel issues the partial loads together and uses independent FP32 accumulation chains;
 // "Expose more parallelism in attention": the combine applies the sink correction and keeps the
 // BF16 rounding boundary (the output is rounded to bf16 once, here).
 #include <cuda_bf16.h>
@@ -10,113 +10,117 @@
 
 namespace va {
 
-constexpr int kCombineWarps = 8;
-constexpr int kCombineThreads = 32 * kCombineWarps;
+constexpr int kCombineThreads = 256;
+constexpr int kQuarters = 4;                       // column quarters of a matrix row: 32 columns each
+constexpr int kChunks = kD / kQuarters / 4;        // float4 chunks per quarter: 8
+constexpr int kGroups = kCombineThreads / kChunks; // split groups: 32
+constexpr int kBatch = 8;                          // splits per thread loaded together
 
-// One CTA per matrix row m = r * 6 + h.  Warp w accumulates the splits s = w, w + 8, ...: each lane owns
-// four output columns and keeps four independent accumulators (one per unrolled split), with the four
-// splits' loads issued before any of them is used.  The eight warp totals are then added in a fixed
-// order.  Shared memory holds the split weights exp(lse_s - L).
+// One CTA per (matrix row m = 6 r + h, column quarter).  Thread t owns float4 chunk t % 8 of the quarter
+// and the splits s = t / 8 + 32 i: it issues all of its partial and LSE loads before using any of them
+// (the partials do not depend on the maximum, so normalisation waits until the end:
+// out = sum_s e^(lse_s - M) o_s / (sum_s e^(lse_s - M) + e^(sink - M)), M the maximum over {lse_s} U {sink}).
+// Every thread keeps its own FP32 chains; the 32 per-chunk totals are added in a fixed order.
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* __restrict__ part_o,
                                                                   const float* __restrict__ part_lse,
                                                                   int n_splits, const float* __restrict__ sink,
                                                                   int n_rows, int n_live,
                                                                   __nv_bfloat16* __restrict__ out,
                                                                   float* __restrict__ out_lse) {
-    extern __shared__ float w[];          // [n_splits]
-    __shared__ float red[kCombineWarps];
-    __shared__ float4 part[kCombineWarps][kD / 4];
-    __shared__ float s_mx, s_L;
-    const int m = blockIdx.x;
+    __shared__ float red[kCombineThreads / 32];
+    __shared__ float4 part[kGroups][kChunks];
+    __shared__ float zpart[kGroups];
+    __shared__ float s_mx;
+    const int m = blockIdx.x, quarter = blockIdx.y;
     const int r = m / kH, h = m - r * kH;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int chunk = tid % kChunks, group = tid / kChunks;
     const int M = n_rows * kH;
+    const int col0 = quarter * (kD / kQuarters) + 4 * chunk;
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();   // every global access comes after this
     if (r >= n_live) {
-        if (tid < kD) out[(long long)m * kD + tid] = __float2bfloat16_rn(0.0f);
-        if (out_lse && tid == 0) out_lse[m] = -INFINITY;
+        if (tid < kD / kQuarters) out[(long long)m * kD + quarter * (kD / kQuarters) + tid] = __float2bfloat16_rn(0.0f);
+        if (out_lse && quarter == 0 && tid == 0) out_lse[m] = -INFINITY;
         return;
     }
     const float sk = sink ? __ldcg(sink + h) : -INFINITY;
 
-    // L = logsumexp({lse_s} U {sink})
-    float mx = sk;
-    for (int s = tid; s < n_splits; s += kCombineThreads) {
-        const float l = __ldcg(part_lse + (long long)s * M + m);
-        w[s] = l;
-        mx = fmaxf(mx, l);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float z = 0.0f, mx = sk;   // running maximum over the splits seen so far and the sink
+    // Splits in batches of kGroups * kBatch (256 for 152 or fewer splits: one batch).
+    for (int base = 0; base < n_splits; base += kGroups * kBatch) {
+        float4 o[kBatch];
+        float l[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int s = base + group + kGroups * i;
+            if (s < n_splits) {
+                l[i] = __ldcg(part_lse + (long long)s * M + m);
+                o[i] = __ldcg(reinterpret_cast<const float4*>(part_o + ((long long)s * M + m) * kD + col0));
+            } else {
+                l[i] = -INFINITY;
+                o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        // maximum over this batch and the sink (whole block), then rescale what was accumulated so far
+        float bm = sk;
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) bm = fmaxf(bm, l[i]);
+        for (int off = 16; off > 0; off >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
+        if (lane == 0) red[warp] = bm;
+        __syncthreads();
+        if (tid == 0) {
+            float t = red[0];
+            for (int i = 1; i < kCombineThreads / 32; ++i) t = fmaxf(t, red[i]);
+            s_mx = t;
+        }
+        __syncthreads();
+        const float nm = fmaxf(mx, s_mx);
+        if (nm != -INFINITY) {
+            const float a = (mx == -INFINITY) ? 0.0f : expf(mx - nm);
+            acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
+            z *= a;
+#pragma unroll
+            for (int i = 0; i < kBatch; ++i) {
+                const float w = (l[i] == -INFINITY) ? 0.0f : expf(l[i] - nm);
+                acc.x = fmaf(w, o[i].x, acc.x);
+                acc.y = fmaf(w, o[i].y, acc.y);
+                acc.z = fmaf(w, o[i].z, acc.z);
+                acc.w = fmaf(w, o[i].w, acc.w);
+                z += w;
+            }
+        }
+        mx = nm;
+        __syncthreads();   // red / s_mx are reused by the next batch
     }
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) red[warp] = mx;
+    part[group][chunk] = acc;
+    if (chunk == 0) zpart[group] = z;
     __syncthreads();
-    if (tid == 0) {
-        float t = red[0];
-        for (int i = 1; i < kCombineWarps; ++i) t = fmaxf(t, red[i]);
-        s_mx = t;
-    }
-    __syncthreads();
-    mx = s_mx;
-    if (mx == -INFINITY) {  // nothing visible and no sink
-        if (tid < kD) out[(long long)m * kD + tid] = __float2bfloat16_rn(0.0f);
-        if (out_lse && tid == 0) out_lse[m] = -INFINITY;
+    if (mx == -INFINITY) {   // nothing visible and no sink
+        if (tid < kD / kQuarters) out[(long long)m * kD + quarter * (kD / kQuarters) + tid] = __float2bfloat16_rn(0.0f);
+        if (out_lse && quarter == 0 && tid == 0) out_lse[m] = -INFINITY;
         return;
     }
-    float z = (tid == 0) ? expf(sk - mx) : 0.0f;
-    for (int s = tid; s < n_splits; s += kCombineThreads) z += expf(w[s] - mx);
-    for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-    if (lane == 0) red[warp] = z;
-    __syncthreads();
-    if (tid == 0) {
-        float zt = 0.0f;
-        for (int i = 0; i < kCombineWarps; ++i) zt += red[i];
-        s_L = mx + logf(zt);
-    }
-    __syncthreads();
-    const float L = s_L;
-    for (int s = tid; s < n_splits; s += kCombineThreads) w[s] = expf(w[s] - L);
-    __syncthreads();
-
-    // out[d] = sum_s w_s o_s[d]
-    const float4* po = reinterpret_cast<const float4*>(part_o + (long long)m * kD) + lane;
-    const long long stride4 = (long long)M * kD / 4;
-    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0, a2 = a0, a3 = a0;
-    int s = warp;
-    for (; s + 3 * kCombineWarps < n_splits; s += 4 * kCombineWarps) {
-        const float4 o0 = __ldcg(po + (long long)(s + 0 * kCombineWarps) * stride4);
-        const float4 o1 = __ldcg(po + (long long)(s + 1 * kCombineWarps) * stride4);
-        const float4 o2 = __ldcg(po + (long long)(s + 2 * kCombineWarps) * stride4);
-        const float4 o3 = __ldcg(po + (long long)(s + 3 * kCombineWarps) * stride4);
-        const float w0 = w[s], w1 = w[s + kCombineWarps], w2 = w[s + 2 * kCombineWarps], w3 = w[s + 3 * kCombineWarps];
-        a0.x = fmaf(w0, o0.x, a0.x); a0.y = fmaf(w0, o0.y, a0.y); a0.z = fmaf(w0, o0.z, a0.z); a0.w = fmaf(w0, o0.w, a0.w);
-        a1.x = fmaf(w1, o1.x, a1.x); a1.y = fmaf(w1, o1.y, a1.y); a1.z = fmaf(w1, o1.z, a1.z); a1.w = fmaf(w1, o1.w, a1.w);
-        a2.x = fmaf(w2, o2.x, a2.x); a2.y = fmaf(w2, o2.y, a2.y); a2.z = fmaf(w2, o2.z, a2.z); a2.w = fmaf(w2, o2.w, a2.w);
-        a3.x = fmaf(w3, o3.x, a3.x); a3.y = fmaf(w3, o3.y, a3.y); a3.z = fmaf(w3, o3.z, a3.z); a3.w = fmaf(w3, o3.w, a3.w);
-    }
-    for (; s < n_splits; s += kCombineWarps) {
-        const float4 o0 = __ldcg(po + (long long)s * stride4);
-        const float w0 = w[s];
-        a0.x = fmaf(w0, o0.x, a0.x); a0.y = fmaf(w0, o0.y, a0.y); a0.z = fmaf(w0, o0.z, a0.z); a0.w = fmaf(w0, o0.w, a0.w);
-    }
-    part[warp][lane] = make_float4((a0.x + a1.x) + (a2.x + a3.x), (a0.y + a1.y) + (a2.y + a3.y),
-                                   (a0.z + a1.z) + (a2.z + a3.z), (a0.w + a1.w) + (a2.w + a3.w));
-    __syncthreads();
-    if (tid < kD) {
-        const float* pf = reinterpret_cast<const float*>(part);
-        float acc = 0.0f;
-#pragma unroll
-        for (int i = 0; i < kCombineWarps; ++i) acc += pf[i * kD + tid];
-        out[(long long)m * kD + tid] = __float2bfloat16_rn(acc);
-        if (out_lse && tid == 0) out_lse[m] = L;
+    if (tid < kD / kQuarters) {
+        const int c = tid >> 2, e = tid & 3;   // output column quarter*32 + tid = chunk c, element e
+        float sum = 0.0f, zt = 0.0f;
+        for (int g = 0; g < kGroups; ++g) {
+            const float4 v = part[g][c];
+            sum += (e == 0) ? v.x : (e == 1) ? v.y : (e == 2) ? v.z : v.w;
+            zt += zpart[g];
+        }
+        zt += (sk == -INFINITY) ? 0.0f : expf(sk - mx);
+        out[(long long)m * kD + quarter * (kD / kQuarters) + tid] = __float2bfloat16_rn(sum / zt);
+        if (out_lse && quarter == 0 && tid == 0) out_lse[m] = mx + logf(zt);
     }
 }
 
 cudaError_t launch_combine(const float* part_o, const float* part_lse, int n_splits, const float* sink,
                            int n_rows, int n_live, uint16_t* out, float* out_lse, cudaStream_t stream) {
-    const size_t smem = sizeof(float) * (size_t)(n_splits > 0 ? n_splits : 1);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    pdl_config(&cfg, attr, dim3(n_rows * kH), dim3(kCombineThreads), smem, stream);
+    pdl_config(&cfg, attr, dim3(n_rows * kH, kQuarters), dim3(kCombineThreads), 0, stream);
     const cudaError_t e = cudaLaunchKernelEx(&cfg, combine_kernel, part_o, part_lse, n_splits, sink, n_rows, n_live,
                                              reinterpret_cast<__nv_bfloat16*>(out), out_lse);
     return e != cudaSuccess ? e : cudaGetLastError();

@@ -19,9 +19,10 @@
 //     waiting on a barrier never holds up another); eight softmax warps, two per TMEM lane quadrant (one
 //     per half of the 48 matrix rows): thread L holds key L of the tile for S^T and output column d = L
 //     for O^T.
-//   * Softmax keeps one reference maximum per matrix row, shared by the CTA.  Scores may exceed it by up
-//     to 2^8 before it is raised (a CTA-wide vote); raising it rescales the TMEM accumulator and the
-//     running sums.  The log-sum-exp stays exact: lse = ref + log2(sum) in base-2 units.
+//   * Softmax keeps one reference per matrix row, shared by the CTA: initially the scaled score of the
+//     split's first key.  Scores may exceed it by up to 2^8 before it is raised to the exact running
+//     maximum (a CTA-wide vote); raising it rescales the TMEM accumulator and the running sums.  The
+//     log-sum-exp stays exact: lse = ref + log2(sum) in base-2 units.
 //   * P is split into bf16 hi + lo parts (two MMAs into the same accumulator), so the probabilities
 //     enter the product with ~2^-17 relative error instead of bf16's 2^-9.
 //   * K/V rows outside the split's owned positions (the unaligned ends of the extent: cache capacity
@@ -54,6 +55,10 @@ namespace tc {
 // them interleaved, so tile 0 lands no earlier than the rest and no stage frees up for several us.
 // Requesting tile j of the first ring fill j * VA_STAGGER_NS after tile 0 lets tile 0 land first.
 // 1.2 us measured best on GB300 (0: no stagger).
+// Tiles pulled into L2 ahead of the rings by the softmax warps with plain loads (0: none).
+#ifndef VA_L2AHEAD
+#define VA_L2AHEAD 0
+#endif
 #ifndef VA_STAGGER_NS
 #define VA_STAGGER_NS 1200
 #endif
@@ -101,6 +106,7 @@ struct Misc {
     float alpha[kMaxM];
     float inv_l[kMaxM];
     long long row_lo[kMaxRows], row_hi[kMaxRows];
+    int pos[kMaxRows];
 };
 constexpr uint32_t kSmemBytes = kOffMisc + (uint32_t)sizeof(Misc) + 1024;
 static_assert(kOffQ % 1024 == 0 && kStage % 1024 == 0 && 2 * kPBytes <= kStage, "swizzle atoms need 1 KB alignment");
@@ -194,6 +200,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
         ptx::mbar_init(bar(ms.drain), 1);
         ms.abort = 0;
         ptx::mbar_init_fence();
+        VA_TRACE_AT(240);
     }
     if (tid == 32) {
         ptx::tma_prefetch_desc(&tmq);
@@ -203,14 +210,22 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
         ptx::tma_prefetch_desc(&tmv2);
     }
     if (warp == 1) ptx::tmem_alloc(ptx::smem_u32(&ms.tmem_base), kTmemCols);
+    if (tid == 32) VA_TRACE_AT(241);
 
     // Programmatic dependent launch: every global access of this kernel comes after griddep_wait.
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
+    if (tid == 0) VA_TRACE_AT(242);
 
+    // the positions: one request per CTA, shared through shared memory
+    if (warp == 0 && lane < a.n_live) ms.pos[lane] = __ldcg(a.pos + lane);
+    __syncthreads();
     int row_pos[kMaxRows];
-    const Plan P = make_plan(a.pos, a.n_live, a.window, a.slots, a.n_splits, split, row_pos);
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) row_pos[r] = (r < a.n_live) ? ms.pos[r] : 0;
+    const Plan P = make_plan(row_pos, a.n_live, a.window, a.slots, a.n_splits, split);
     if (P.status && split == 0 && tid == 0 && a.dev_status) atomicOr(a.dev_status, P.status);
+    if (tid == 0) VA_TRACE_AT(243);
     const int n64 = P.status ? 0 : (int)(P.t1 - P.t0);
     const int ntiles = (n64 + 1) >> 1;
     float* part_o = a.part_o + (long long)split * M * kD;
@@ -365,13 +380,20 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
             constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, 48, 0, 0);   // A = K, B = Q: both K-major
             constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, 48, 1, 1);   // A = V^T, B = P^T: MN-major
             bool ok = ptx::mbar_wait(bar(ms.q_full), 0, abort_flag, kWaitNs);
-            for (int j = 0; j <= ntiles && ok; ++j) {
-                if (j < ntiles) {
-                    const int ks = j % kNK, sb = j & 1;
-                    ok = ptx::mbar_wait(bar(ms.k_full[ks]), (j / kNK) & 1, abort_flag, kWaitNs) &&
-                         ptx::mbar_wait(bar(ms.s_free[sb]), ((j >> 1) & 1) ^ 1, abort_flag, kWaitNs);
-                    if (!ok) break;
-                    VA_TRACE_TILE(j, 2);
+            // Issue whichever product is ready: QK(qk) once K(qk) has landed and its S buffer is free, and
+            // PV(pv) once V(pv) has landed and P(pv) is published.  PV never waits for a later K, so the
+            // stages of tile pv return to the rings as soon as possible.  QK(j) is issued only after PV(j-2):
+            // the commit after QK(j) then covers PV(j-2), which keeps every parity wait at most one phase
+            // behind its barrier.
+            int qk = 0, pv = 0;
+            uint64_t idle_since = 0;
+            while (ok && pv < ntiles) {
+                bool progressed = false;
+                if (qk < ntiles && qk <= pv + 1 &&
+                    ptx::mbar_test_wait(bar(ms.k_full[qk % kNK]), (qk / kNK) & 1) &&
+                    ptx::mbar_test_wait(bar(ms.s_free[qk & 1]), ((qk >> 1) & 1) ^ 1)) {
+                    const int ks = qk % kNK, sb = qk & 1;
+                    VA_TRACE_TILE(qk, 2);
                     ptx::tc_fence_after();
                     const uint32_t d = tmem + (sb ? kColS1 : kColS0);
 #pragma unroll
@@ -381,14 +403,14 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
                                       ptx::smem_desc(base_s + kOffQ + h * kQHalf + off, 0, 1024), idesc_qk, kk > 0);
                     }
                     ptx::mma_commit(bar(ms.s_full[sb]));
+                    ++qk;
+                    progressed = true;
                 }
-                if (j >= 1) {
-                    const int i = j - 1, vs = i % kNV, ps = i % kNK;
-                    ok = ptx::mbar_wait(bar(ms.v_full[vs]), (i / kNV) & 1, abort_flag, kWaitNs);
+                if (pv < qk && ptx::mbar_test_wait(bar(ms.v_full[pv % kNV]), (pv / kNV) & 1) &&
+                    ptx::mbar_test_wait(bar(ms.p_full[pv & 1]), (pv >> 1) & 1)) {
+                    const int i = pv, vs = i % kNV, ps = i % kNK;
                     VA_TRACE_TILE(i, 3);
-                    ok = ok && ptx::mbar_wait(bar(ms.p_full[i & 1]), (i >> 1) & 1, abort_flag, kWaitNs);
                     VA_TRACE_TILE(i, 6);
-                    if (!ok) break;
                     ptx::tc_fence_after();
                     const long long t = tile_t(i);
                     const int nk = (t + 1 < P.t1) ? 8 : 4;
@@ -404,6 +426,15 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
                     ptx::mma_commit(bar(ms.v_empty[vs]));
                     ptx::mma_commit(bar(ms.k_empty[ps]));
                     if (i == ntiles - 1) ptx::mma_commit(bar(ms.o_ready));   // the accumulator is final
+                    ++pv;
+                    progressed = true;
+                }
+                if (progressed) {
+                    idle_since = 0;
+                } else {   // bounded: give up after kWaitNs without progress, or when another role aborted
+                    const uint64_t now = ptx::globaltimer_ns();
+                    if (idle_since == 0) idle_since = now;
+                    if (*abort_flag || now - idle_since > kWaitNs) ok = false;
                 }
             }
             if (!ok) fail();
@@ -431,6 +462,19 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
             ref[i] = ms.ref[n0 + i];
             l[i] = 0.0f;
         }
+        // L2 warm-up of tile jt: softmax thread st touches one 256-byte row of K (st < 128) or V
+        auto l2_touch_tile = [&](int jt) {
+            if (jt >= ntiles) return;
+            int s0, s1, halves;
+            tile_slots(jt, s0, s1, halves);
+            const int st = sw * 32 + lane, r = st & 127, hh = r >> 6;
+            if (hh < halves) {
+                const int row = (hh ? s1 : s0) + (r & 63);
+                if (row < a.slots) ptx::touch_l2_256((st < 128 ? a.k : a.v) + (size_t)row * kD);
+            }
+        };
+        if (VA_L2AHEAD > 0)
+            for (int jt = 1; jt <= VA_L2AHEAD; ++jt) l2_touch_tile(jt);
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
             const long long t = tile_t(j);
@@ -438,6 +482,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
             const long long kbase = t * kTile;
             const long long kp = kbase + L;
             const int sb = j & 1;
+            if (VA_L2AHEAD > 0 && j > 0) l2_touch_tile(j + VA_L2AHEAD);
             if (!ptx::mbar_wait(bar(ms.s_full[sb]), (j >> 1) & 1, abort_flag, kWaitNs)) ok = false;
             if (sw == 0 && lane == 0) VA_TRACE_TILE(j, 4);
             ptx::tc_fence_after();
@@ -460,6 +505,19 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
 #pragma unroll
                 for (int i = 0; i < kCols; ++i) vis[i] = rv[i / kH];
             }
+            if (j == 0) {
+                // Initial reference of each row: the scaled score of the split's first key when that key
+                // is visible to the row (thread L = 0 holds it), else -inf-like, which forces the exact
+                // rescale below.  Any later score more than 2^8 above the reference raises it.
+                if (L == 0) {
+#pragma unroll
+                    for (int i = 0; i < kCols; ++i)
+                        if (n0 + i < ML) ms.ref[n0 + i] = vis[i] ? x[i] * c : kRefInit;
+                }
+                ptx::named_bar_sync(1, kSoftThreads);
+#pragma unroll
+                for (int i = 0; i < kCols; ++i) ref[i] = ms.ref[n0 + i];
+            }
             float p[kCols];
             float pmax = 0.0f;
 #pragma unroll
@@ -471,6 +529,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
             const unsigned want = __any_sync(0xffffffffu, !(pmax <= kThresh));
             if (lane == 0) ms.vote[j & 1][sw] = want ? 1 : 0;
             ptx::named_bar_sync(1, kSoftThreads);
+            if (j == 0 && sw == 0 && lane == 0) VA_TRACE_AT(250);
             int any = 0;
 #pragma unroll
             for (int w = 0; w < kSoftWarps; ++w) any |= ms.vote[j & 1][w];
@@ -497,6 +556,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
                     ms.ref[L] = nw;
                 }
                 ptx::named_bar_sync(1, kSoftThreads);
+                if (j == 0 && sw == 0 && lane == 0) VA_TRACE_AT(251);
 #pragma unroll
                 for (int i = 0; i < kCols; ++i) {
                     ref[i] = ms.ref[n0 + i];
@@ -525,6 +585,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
                 hi_w[i] = hb;
                 lo_w[i] = pack_bf16x2(p0 - __uint_as_float(hb << 16), p1 - __uint_as_float(hb & 0xFFFF0000u));
             }
+            if (j == 0 && sw == 0 && lane == 0) VA_TRACE_AT(252);
             // V rows of positions this split does not own are zeroed before PV reads them (column half ch)
             const int vs = j % kNV;
             if (kbase < own_lo || kbase + nkeys > own_hi) {
@@ -549,6 +610,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
                         make_uint4(lo_w[4 * k], lo_w[4 * k + 1], lo_w[4 * k + 2], lo_w[4 * k + 3]);
                 }
             }
+            if (j == 0 && sw == 0 && lane == 0) VA_TRACE_AT(253);
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             __syncwarp();

@@ -41,6 +41,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
+// Non-blocking check that the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Gives up (returns false) after
 // `limit_ns` nanoseconds, or at once when *abort becomes non-zero.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const volatile int* abort,
@@ -82,6 +93,13 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
+}
+
+// A 4-byte load that asks L2 to fetch the whole 256-byte block around it (LSU path, not the TMA
+// engine); the value is discarded.
+__device__ __forceinline__ void touch_l2_256(const void* gaddr) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L2::256B.b32 %0, [%1];" : "=r"(v) : "l"(reinterpret_cast<uint64_t>(gaddr)) : "memory");
 }
 
 // Prefetch `bytes` (a multiple of 16) of contiguous global memory into L2.

@@ -36,14 +36,14 @@ struct Plan {
     int status;            // VA_DEV_* bits, 0 if the positions are usable
 };
 
-// Also returns the live rows' positions in row_pos[] (entries past n_live are 0).
-__device__ __forceinline__ Plan make_plan(const int32_t* __restrict__ pos, int n_live, int window,
-                                          int slots, int n_splits, int split, int (&row_pos)[kMaxRows]) {
+// row_pos[] holds the live rows' positions (entries past n_live are ignored).  Callers load them once
+// per CTA (one request) and share them: every thread of every CTA loading the same eight integers
+// turns one L2 line into a hot spot that costs microseconds.
+__device__ __forceinline__ Plan make_plan(const int (&row_pos)[kMaxRows], int n_live, int window, int slots,
+                                          int n_splits, int split) {
     Plan P;
     P.lo = P.hi = P.t0 = P.t1 = 0;
     P.status = 0;
-#pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) row_pos[r] = (r < n_live) ? __ldcg(pos + r) : 0;
     if (n_live <= 0) return P;
     const int p0 = row_pos[0];
     int prev = p0, last = p0;

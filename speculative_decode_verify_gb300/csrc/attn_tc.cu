@@ -59,6 +59,15 @@ namespace tc {
 #ifndef VA_L2AHEAD
 #define VA_L2AHEAD 0
 #endif
+#ifndef VA_HINT_KV
+#define VA_HINT_KV 1
+#endif
+#ifndef VA_HINT_POS
+#define VA_HINT_POS 1
+#endif
+#ifndef VA_HINT_Q
+#define VA_HINT_Q 1
+#endif
 #ifndef VA_STAGGER_NS
 #define VA_STAGGER_NS 1200
 #endif
@@ -218,7 +227,8 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
     if (tid == 0) VA_TRACE_AT(242);
 
     // the positions: one request per CTA, shared through shared memory
-    if (warp == 0 && lane < a.n_live) ms.pos[lane] = __ldcg(a.pos + lane);
+    if (warp == 0 && lane < a.n_live)
+        ms.pos[lane] = VA_HINT_POS ? ptx::ld_int_policy(a.pos + lane, ptx::policy_evict_last()) : __ldcg(a.pos + lane);
     __syncthreads();
     int row_pos[kMaxRows];
 #pragma unroll
@@ -257,16 +267,25 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
     };
     // K/V of tile j into its ring stage: per 64-column half one 128-row box (contiguous halves) or one
     // 64-row box per half.  A load also prefetches tile j + kPrefetch into L2.
+    // K/V are read once: evict-first, so that they do not push the small per-call inputs out of L2
     auto load_tile = [&](const CUtensorMap* m64, const CUtensorMap* m128, uint32_t stage, uint64_t& full, int j) {
         int s0, s1, halves;
         tile_slots(j, s0, s1, halves);
+        const uint64_t pol = ptx::policy_evict_first();
         ptx::mbar_arrive_expect_tx(bar(full), (uint32_t)halves * 2u * kHalfBox);
         if (halves == 2 && s1 == s0 + kTile) {
-            for (int h = 0; h < 2; ++h) ptx::tma_load_2d(stage + h * kDHalf, m128, h * 64, s0, bar(full));
+            for (int h = 0; h < 2; ++h) {
+                if (VA_HINT_KV) ptx::tma_load_2d_hint(stage + h * kDHalf, m128, h * 64, s0, bar(full), pol);
+                else ptx::tma_load_2d(stage + h * kDHalf, m128, h * 64, s0, bar(full));
+            }
         } else {
             for (int hh = 0; hh < halves; ++hh)
-                for (int h = 0; h < 2; ++h)
-                    ptx::tma_load_2d(stage + h * kDHalf + hh * kHalfBox, m64, h * 64, hh ? s1 : s0, bar(full));
+                for (int h = 0; h < 2; ++h) {
+                    if (VA_HINT_KV)
+                        ptx::tma_load_2d_hint(stage + h * kDHalf + hh * kHalfBox, m64, h * 64, hh ? s1 : s0, bar(full), pol);
+                    else
+                        ptx::tma_load_2d(stage + h * kDHalf + hh * kHalfBox, m64, h * 64, hh ? s1 : s0, bar(full));
+                }
         }
     };
     auto load_k = [&](int j) {
@@ -294,8 +313,14 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
         if (tid == 0) {
             // Q, then the first stages
             ptx::mbar_arrive_expect_tx(bar(ms.q_full), kQBytes);
-            ptx::tma_load_2d(base_s + kOffQ, &tmq, 0, 0, bar(ms.q_full));
-            ptx::tma_load_2d(base_s + kOffQ + kQHalf, &tmq, 64, 0, bar(ms.q_full));
+            const uint64_t keep = ptx::policy_evict_last();   // every CTA reads the same q
+            if (VA_HINT_Q) {
+                ptx::tma_load_2d_hint(base_s + kOffQ, &tmq, 0, 0, bar(ms.q_full), keep);
+                ptx::tma_load_2d_hint(base_s + kOffQ + kQHalf, &tmq, 64, 0, bar(ms.q_full), keep);
+            } else {
+                ptx::tma_load_2d(base_s + kOffQ, &tmq, 0, 0, bar(ms.q_full));
+                ptx::tma_load_2d(base_s + kOffQ + kQHalf, &tmq, 64, 0, bar(ms.q_full));
+            }
             ms.t_first = ptx::globaltimer_ns();
             for (int j = 0; j < k_first; ++j) load_k(j);
             for (int j = 0; j < v_first; ++j) load_v(j);

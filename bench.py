@@ -60,6 +60,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the 1K-192K context sweep")
     ap.add_argument("--splits", type=int, default=0, help="split count (0 = library policy)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="profiling aid: only the split-attention launches, over --caches rotating caches")
@@ -316,6 +317,69 @@ def ours(args, dist: Dist):
         for c in calls:
             launch_call(c)
 
+    def sweep_point(ctx, window, reps=200):
+        """us per call and algorithmic GB/s of one verify call (append + attention + combine, graph
+        replay) at this context; two caches alternate so K/V are read cold when they exceed L2."""
+        n = 8
+        ws = []
+        for rep in range(2):
+            w = synth.make(f"sweep{ctx}", 900 + rep, ctx=ctx, n_live=n, window=window,
+                           slots=(synth.RING_SLOTS if window else ctx + 64))
+            slots = w.slots
+            k = torch.full((slots, 128), synth.BF16_NAN, dtype=torch.int16)
+            v = torch.full((slots, 128), synth.BF16_NAN, dtype=torch.int16)
+            kb, vb = synth.bits(w.k_hist), synth.bits(w.v_hist)
+            first = max(0, ctx - slots) if window else 0
+            pp = torch.arange(first, ctx)
+            k[pp % slots] = kb[first:ctx]
+            v[pp % slots] = vb[first:ctx]
+            idx = w.pos[:n].to(torch.int64)
+            ws.append(dict(w=w, k=k.to(dev), v=v.to(dev), q=synth.bits(w.q).to(dev), pos=w.pos.to(dev),
+                           sink=w.sink.to(dev), kn=kb[idx].contiguous().to(dev), vn=vb[idx].contiguous().to(dev),
+                           out=torch.empty(8, 6, 128, dtype=torch.int16, device=dev)))
+        Ss = va.va_auto_splits(window + n - 1 if window else ctx, window)
+        po = torch.empty(Ss, 8, 6, 128, dtype=torch.float32, device=dev)
+        pl = torch.empty(Ss, 8, 6, dtype=torch.float32, device=dev)
+
+        def one(c):
+            w = c["w"]
+            st = L.kv_ring_append(P(c["kn"].data_ptr()), P(c["vn"].data_ptr()), n, P(c["k"].data_ptr()),
+                                  P(c["v"].data_ptr()), w.slots, P(c["pos"].data_ptr()), None, sp)
+            if window:
+                st |= L.verify_attn_swa(P(c["q"].data_ptr()), 8, n, P(c["k"].data_ptr()), P(c["v"].data_ptr()),
+                                        w.slots, window, P(c["pos"].data_ptr()), ctypes.c_float(w.scale), Ss,
+                                        P(po.data_ptr()), P(pl.data_ptr()), None, None, sp)
+            else:
+                st |= L.verify_attn_full(P(c["q"].data_ptr()), 8, n, P(c["k"].data_ptr()), P(c["v"].data_ptr()),
+                                         w.slots, P(c["pos"].data_ptr()), ctypes.c_float(w.scale), Ss,
+                                         P(po.data_ptr()), P(pl.data_ptr()), None, None, sp)
+            st |= L.attn_split_combine(P(po.data_ptr()), P(pl.data_ptr()), Ss, P(c["sink"].data_ptr()), 8, n,
+                                       P(c["out"].data_ptr()), None, sp)
+            if st:
+                raise RuntimeError(f"sweep call failed with status {st}")
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                for c in ws:
+                    one(c)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for c in ws:
+                    one(c)
+            g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * 2)
+        hi = ctx
+        lo = max(0, ctx - n - window + 1) if window else 0
+        nbytes = 512 * (hi - lo) + Q_BYTES + OUT_BYTES + 2 * 512 * n + 24
+        return {"ctx": ctx, "kind": "swa" if window else "full", "n_live": n, "splits": Ss, "us_per_call": us,
+                "gbs": nbytes / us / 1e3}
+
     if args.kernel_only:
         # the split-attention kernel alone, back to back over the rotating caches (for ncu captures)
         with torch.cuda.stream(stream):
@@ -419,6 +483,11 @@ def ours(args, dist: Dist):
         dist.barrier()
     clk = clocks.stop()
 
+    sweep = []
+    if not args.no_sweep:
+        for ctx_s in synth.SWEEP_CONTEXTS:
+            for window in (0, synth.WINDOW):
+                sweep.append(sweep_point(ctx_s, window))
     step_bytes = sum(call_bytes(c["hi"], c["n"]) for c in calls)
     value, t_max = aggregate(step_bytes * args.steps / 1e9, t_graph, dist)
     e2e_value, _ = aggregate(step_bytes * ke / 1e9, t_e2e, dist)
@@ -449,6 +518,7 @@ def ours(args, dist: Dist):
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "us_per_step": t_e2e / ke * 1e6},
         "gpu_launches": 3 * len(calls) * args.steps,
+        "sweep": [{k: (round(v, 2) if isinstance(v, float) else v) for k, v in p.items()} for p in sweep],
         "clocks": clk,
     }
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:

@@ -102,17 +102,28 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* _
         if (out_lse && quarter == 0 && tid == 0) out_lse[m] = -INFINITY;
         return;
     }
-    if (tid < kD / kQuarters) {
-        const int c = tid >> 2, e = tid & 3;   // output column quarter*32 + tid = chunk c, element e
+    // Totals: output column o = 4 c + e (32 per quarter) is summed over the 32 groups by the 8 threads
+    // 8 o .. 8 o + 7 (four groups each, then a fixed xor-shuffle tree); the 32 partial sums of z likewise.
+    {
+        const int o = tid >> 3, k = tid & 7, c = o >> 2, e = o & 3;
         float sum = 0.0f, zt = 0.0f;
-        for (int g = 0; g < kGroups; ++g) {
+#pragma unroll
+        for (int i = 0; i < kGroups / 8; ++i) {
+            const int g = k + 8 * i;
             const float4 v = part[g][c];
             sum += (e == 0) ? v.x : (e == 1) ? v.y : (e == 2) ? v.z : v.w;
             zt += zpart[g];
         }
-        zt += (sk == -INFINITY) ? 0.0f : expf(sk - mx);
-        out[(long long)m * kD + quarter * (kD / kQuarters) + tid] = __float2bfloat16_rn(sum / zt);
-        if (out_lse && quarter == 0 && tid == 0) out_lse[m] = mx + logf(zt);
+#pragma unroll
+        for (int off = 4; off > 0; off >>= 1) {
+            sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            zt += __shfl_xor_sync(0xffffffffu, zt, off);
+        }
+        if (k == 0) {
+            zt += (sk == -INFINITY) ? 0.0f : expf(sk - mx);
+            out[(long long)m * kD + quarter * (kD / kQuarters) + o] = __float2bfloat16_rn(sum / zt);
+            if (out_lse && quarter == 0 && o == 0) out_lse[m] = mx + logf(zt);
+        }
     }
 }
 

@@ -17,20 +17,20 @@ constexpr int kGroups = kCombineThreads / kChunks; // split groups: 32
 constexpr int kBatch = 8;                          // splits per thread loaded together
 
 // One CTA per (matrix row m = 6 r + h, column quarter).  Thread t owns float4 chunk t % 8 of the quarter
-// and the splits s = t / 8 + 32 i: it issues all of its partial and LSE loads before using any of them
-// (the partials do not depend on the maximum, so normalisation waits until the end:
-// out = sum_s e^(lse_s - M) o_s / (sum_s e^(lse_s - M) + e^(sink - M)), M the maximum over {lse_s} U {sink}).
-// Every thread keeps its own FP32 chains; the 32 per-chunk totals are added in a fixed order.
+// and the splits s = t / 8 + 32 i: it issues all of its partial and LSE loads before using any of them.
+// Each warp merges its own splits against its own maximum (a two-level log-sum-exp merge), so the CTA
+// needs one barrier: the warp totals are then rescaled to the CTA maximum (which includes the sink) and
+// added in a fixed order: out = sum_s e^(lse_s - M) o_s / (sum_s e^(lse_s - M) + e^(sink - M)).
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* __restrict__ part_o,
                                                                   const float* __restrict__ part_lse,
                                                                   int n_splits, const float* __restrict__ sink,
                                                                   int n_rows, int n_live,
                                                                   __nv_bfloat16* __restrict__ out,
                                                                   float* __restrict__ out_lse) {
-    __shared__ float red[kCombineThreads / 32];
-    __shared__ float4 part[kGroups][kChunks];
-    __shared__ float zpart[kGroups];
-    __shared__ float s_mx;
+    constexpr int kWarps = kCombineThreads / 32;
+    __shared__ float4 part[kWarps][kChunks];   // per warp, per chunk: weighted sums (against the warp max)
+    __shared__ float zpart[kWarps];            // per warp: sum of weights
+    __shared__ float wmax[kWarps];             // per warp: its maximum lse
     const int m = blockIdx.x, quarter = blockIdx.y;
     const int r = m / kH, h = m - r * kH;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -47,8 +47,7 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* _
     const float sk = sink ? __ldcg(sink + h) : -INFINITY;
 
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float z = 0.0f, mx = sk;   // running maximum over the splits seen so far and the sink
-    // Splits in batches of kGroups * kBatch (256 for 152 or fewer splits: one batch).
+    float z = 0.0f, mx = -INFINITY;   // this warp's running maximum over the splits it has merged
     for (int base = 0; base < n_splits; base += kGroups * kBatch) {
         float4 o[kBatch];
         float l[kBatch];
@@ -63,67 +62,65 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* _
                 o[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
-        // maximum over this batch and the sink (whole block), then rescale what was accumulated so far
-        float bm = sk;
+        float bm = mx;
 #pragma unroll
         for (int i = 0; i < kBatch; ++i) bm = fmaxf(bm, l[i]);
         for (int off = 16; off > 0; off >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
-        if (lane == 0) red[warp] = bm;
-        __syncthreads();
-        if (tid == 0) {
-            float t = red[0];
-            for (int i = 1; i < kCombineThreads / 32; ++i) t = fmaxf(t, red[i]);
-            s_mx = t;
-        }
-        __syncthreads();
-        const float nm = fmaxf(mx, s_mx);
-        if (nm != -INFINITY) {
-            const float a = (mx == -INFINITY) ? 0.0f : expf(mx - nm);
+        if (bm != -INFINITY) {
+            const float a = (mx == -INFINITY) ? 0.0f : expf(mx - bm);
             acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
             z *= a;
 #pragma unroll
             for (int i = 0; i < kBatch; ++i) {
-                const float w = (l[i] == -INFINITY) ? 0.0f : expf(l[i] - nm);
+                const float w = (l[i] == -INFINITY) ? 0.0f : expf(l[i] - bm);
                 acc.x = fmaf(w, o[i].x, acc.x);
                 acc.y = fmaf(w, o[i].y, acc.y);
                 acc.z = fmaf(w, o[i].z, acc.z);
                 acc.w = fmaf(w, o[i].w, acc.w);
                 z += w;
             }
+            mx = bm;
         }
-        mx = nm;
-        __syncthreads();   // red / s_mx are reused by the next batch
     }
-    part[group][chunk] = acc;
-    if (chunk == 0) zpart[group] = z;
+    // within the warp: lanes with the same chunk (lane % 8) hold different splits -> add them
+#pragma unroll
+    for (int off = 8; off < 32; off <<= 1) {
+        acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+        acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
+        acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
+        acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
+        z += __shfl_xor_sync(0xffffffffu, z, off);
+    }
+    if (lane < kChunks) part[warp][lane] = acc;
+    if (lane == 0) {
+        zpart[warp] = z;
+        wmax[warp] = mx;
+    }
     __syncthreads();
-    if (mx == -INFINITY) {   // nothing visible and no sink
-        if (tid < kD / kQuarters) out[(long long)m * kD + quarter * (kD / kQuarters) + tid] = __float2bfloat16_rn(0.0f);
-        if (out_lse && quarter == 0 && tid == 0) out_lse[m] = -INFINITY;
-        return;
-    }
-    // Totals: output column o = 4 c + e (32 per quarter) is summed over the 32 groups by the 8 threads
-    // 8 o .. 8 o + 7 (four groups each, then a fixed xor-shuffle tree); the 32 partial sums of z likewise.
-    {
-        const int o = tid >> 3, k = tid & 7, c = o >> 2, e = o & 3;
-        float sum = 0.0f, zt = 0.0f;
+    // totals: thread o < 32 owns output column quarter*32 + o = chunk o/4, element o%4
+    if (tid < kD / kQuarters) {
+        const int c = tid >> 2, e = tid & 3;
+        float M_ = sk;
 #pragma unroll
-        for (int i = 0; i < kGroups / 8; ++i) {
-            const int g = k + 8 * i;
-            const float4 v = part[g][c];
-            sum += (e == 0) ? v.x : (e == 1) ? v.y : (e == 2) ? v.z : v.w;
-            zt += zpart[g];
+        for (int w = 0; w < kWarps; ++w) M_ = fmaxf(M_, wmax[w]);
+        float* dst_lse = (out_lse && quarter == 0 && tid == 0) ? out_lse + m : nullptr;
+        __nv_bfloat16* dst = out + (long long)m * kD + quarter * (kD / kQuarters) + tid;
+        if (M_ == -INFINITY) {   // nothing visible and no sink
+            *dst = __float2bfloat16_rn(0.0f);
+            if (dst_lse) *dst_lse = -INFINITY;
+            return;
         }
+        float sum = 0.0f, zt = (sk == -INFINITY) ? 0.0f : expf(sk - M_);
 #pragma unroll
-        for (int off = 4; off > 0; off >>= 1) {
-            sum += __shfl_xor_sync(0xffffffffu, sum, off);
-            zt += __shfl_xor_sync(0xffffffffu, zt, off);
+        for (int w = 0; w < kWarps; ++w) {
+            if (wmax[w] == -INFINITY) continue;
+            const float a = expf(wmax[w] - M_);
+            const float4 v = part[w][c];
+            sum = fmaf(a, (e == 0) ? v.x : (e == 1) ? v.y : (e == 2) ? v.z : v.w, sum);
+            zt = fmaf(a, zpart[w], zt);
         }
-        if (k == 0) {
-            zt += (sk == -INFINITY) ? 0.0f : expf(sk - mx);
-            out[(long long)m * kD + quarter * (kD / kQuarters) + o] = __float2bfloat16_rn(sum / zt);
-            if (out_lse && quarter == 0 && o == 0) out_lse[m] = mx + logf(zt);
-        }
+        *dst = __float2bfloat16_rn(sum / zt);
+        if (dst_lse) *dst_lse = M_ + logf(zt);
     }
 }
 

@@ -45,6 +45,7 @@ __all__ = [
     "HEAD_DIM", "Q_HEADS", "TILE", "build", "read_extent", "split_plan", "split_position_ranges",
     "verify_attn", "combine", "ring_slot", "ring_append", "ring_labels", "rows_window_complete",
     "visible_positions", "visible_slot_counts", "bf16_bits_to_f64", "f64_to_bf16_bits",
+    "tree_masks_from_parents", "tree_depths", "tree_extent", "tree_visible_positions", "verify_attn_tree",
 ]
 
 HEAD_DIM = 128
@@ -81,6 +82,10 @@ def _load():
             lib.oracle_verify_attn.argtypes = [p, p, p, ctypes.c_int64, p, ctypes.c_int, ctypes.c_int, p,
                                                ctypes.c_double, ctypes.c_int64, ctypes.c_int, p, p,
                                                p, p, p, p, ctypes.c_int]
+            lib.oracle_verify_attn_tree.restype = ctypes.c_int
+            lib.oracle_verify_attn_tree.argtypes = [p, p, p, ctypes.c_int64, p, ctypes.c_int, ctypes.c_int, p,
+                                                    ctypes.c_double, ctypes.c_int64, ctypes.c_int, p, p,
+                                                    p, p, p, p, ctypes.c_int]
             lib.oracle_combine.restype = ctypes.c_int
             lib.oracle_combine.argtypes = [p, p, ctypes.c_int, p, ctypes.c_int, ctypes.c_int, p, p]
             _lib = lib
@@ -200,6 +205,89 @@ def visible_slot_counts(pos, n_live: int, n_rows: int, window: int, slots: int):
         vis = np.arange(visible_positions(int(pos[r]), window).start, int(pos[r]) + 1, dtype=np.int64)
         np.add.at(cnt[r], vis % slots, 1)
     return cnt
+
+
+# ----------------------------------------------------------------------------- verify trees
+# "Qwen3.8-27B on one RTX 4090", section "More tokens per round: verify trees": the draft is a tree
+# verified in one pass with a tree attention mask.  Node i's K/V sit in slot base + i; node i sees the
+# committed prefix and its ancestors (and itself).
+def tree_masks_from_parents(parents):
+    """Ancestor-or-self bitmasks from a parent array (parents[0] = -1 for the root, parents[i] < i)."""
+    masks = []
+    for i, par in enumerate(parents):
+        par = int(par)
+        assert par < i, "nodes are listed parents first"
+        masks.append((1 << i) | (masks[par] if par >= 0 else 0))
+    return np.array(masks, dtype=np.int32)
+
+
+def tree_depths(masks):
+    """Depth of each node: the number of its strict ancestors."""
+    return np.array([bin(int(m) & 0x7FFFFFFF).count("1") - 1 for m in masks], dtype=np.int64)
+
+
+def tree_extent(base: int, masks, n_nodes: int, window: int = 0):
+    """[lo, hi): the slots the live nodes can see.  hi = base + n_nodes (the node slots); lo = 0 for full
+    attention, else the earliest window start over the nodes (a node at depth d has logical position
+    base + d and a window of W positions ending there), never above base."""
+    if n_nodes <= 0:
+        return 0, 0
+    hi = base + n_nodes
+    if window <= 0:
+        return 0, hi
+    d_min = int(tree_depths(masks[:n_nodes]).min())
+    return min(base, max(0, base + d_min - window + 1)), hi
+
+
+def tree_visible_positions(base: int, masks, n_nodes: int, i: int, window: int = 0):
+    """Sorted slot positions node i sees: its window of the prefix, then its in-window ancestors' slots."""
+    depth = tree_depths(masks[:n_nodes])
+    first = max(0, base + int(depth[i]) - window + 1) if window > 0 else 0
+    out = list(range(min(first, base), base))
+    for k in range(n_nodes):
+        if (int(masks[i]) >> k) & 1 and (window <= 0 or depth[k] >= depth[i] - window + 1):
+            out.append(base + k)
+    return out
+
+
+def verify_attn_tree(q_bits, k_hist_bits, v_hist_bits, base: int, masks, n_nodes: int, sink, scale: float,
+                     window: int = 0, n_splits: int = 0, split_ranges=None, n_threads: int = 1):
+    """FP64 tree verify attention over the linear history (slot j of the history = position j; the nodes
+    at base .. base + n_nodes - 1).  q_bits [n_rows, 6, 128]; masks [>= n_nodes] ancestor-or-self masks.
+    With n_splits > 0 the partials follow ``split_ranges`` (default: the tile plan of ``tree_extent``).
+    Returns dict(out, lse, part_o, part_lse, ranges)."""
+    q = _bits16(q_bits)
+    kh = _bits16(k_hist_bits)
+    vh = _bits16(v_hist_bits)
+    n_rows = q.shape[0]
+    assert q.shape == (n_rows, Q_HEADS, HEAD_DIM) and kh.shape == vh.shape and kh.shape[1] == HEAD_DIM
+    tree = np.zeros(1 + n_rows, dtype=np.int32)
+    tree[0] = base
+    tree[1:1 + n_nodes] = np.asarray(masks, dtype=np.int64)[:n_nodes]
+    sk = None if sink is None else np.ascontiguousarray(np.asarray(sink, dtype=np.float64))
+    if n_splits > 0 and split_ranges is None:
+        lo, hi = tree_extent(base, tree[1:], n_nodes, window)
+        split_ranges = split_position_ranges(lo, hi, n_splits)
+    if split_ranges is None:
+        split_ranges = []
+    S = len(split_ranges)
+    sa = np.ascontiguousarray(np.array([a for a, _ in split_ranges] or [0], dtype=np.int64))
+    sb = np.ascontiguousarray(np.array([b for _, b in split_ranges] or [0], dtype=np.int64))
+    out = np.zeros((n_rows, Q_HEADS, HEAD_DIM), dtype=np.float64)
+    lse = np.zeros((n_rows, Q_HEADS), dtype=np.float64)
+    part_o = np.zeros((max(S, 1), n_rows, Q_HEADS, HEAD_DIM), dtype=np.float64)
+    part_lse = np.zeros((max(S, 1), n_rows, Q_HEADS), dtype=np.float64)
+    rc = _load().oracle_verify_attn_tree(_ptr(q), _ptr(kh), _ptr(vh), kh.shape[0], _ptr(tree), n_rows, n_nodes,
+                                         _ptr(sk), float(scale), int(window), S, _ptr(sa), _ptr(sb),
+                                         _ptr(out), _ptr(lse), _ptr(part_o), _ptr(part_lse), int(n_threads))
+    if rc != 0:
+        raise ValueError(f"oracle_verify_attn_tree rejected its arguments (rc={rc})")
+    return dict(out=out, lse=lse, part_o=part_o[:S], part_lse=part_lse[:S], ranges=list(split_ranges))
+
+
+def _bits16(a):
+    a = np.asarray(a)
+    return np.ascontiguousarray(a.view(np.uint16) if a.dtype == np.int16 else a.astype(np.uint16))
 
 
 # ----------------------------------------------------------------------------- fp64 attention

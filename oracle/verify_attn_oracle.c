@@ -63,6 +63,7 @@ typedef struct {
     const double *sink; /* may be NULL: no sink */
     double scale;
     int64_t window;     /* 0: full attention */
+    const int32_t *tree; /* NULL, or tree verify: tree[0] = base slot, tree[1 + r] = ancestor mask of node r */
     int n_splits;
     const int64_t *split_a, *split_b; /* [n_splits] position ranges, may be NULL if n_splits == 0 */
     double *out, *lse, *part_o, *part_lse;
@@ -70,17 +71,58 @@ typedef struct {
     pthread_mutex_t mu;
 } job_t;
 
-/* Attention of one live (row, head) pair over its whole visible set. */
+/* Depth of a tree node: the number of its strict ancestors (bits of its mask other than its own). */
+static int tree_depth(int32_t mask)
+{
+    int n = 0;
+    for (int b = 0; b < 31; ++b) n += (mask >> b) & 1;
+    return n - 1;
+}
+
+/* First prefix position a row may see: 0 for full attention, else the start of its window.  A tree
+ * node's window ends at its own logical position base + depth (the slot index of the node plays no part). */
+static int64_t row_first(const job_t *J, int r)
+{
+    if (J->window <= 0) return 0;
+    const int64_t p = J->tree ? (int64_t)J->tree[0] + tree_depth(J->tree[1 + r]) : (int64_t)J->pos[r];
+    return p - J->window + 1 > 0 ? p - J->window + 1 : 0;
+}
+
+/* Is key j visible to row r?  Plain definitions:
+ *   chain:  row_first(r) <= j <= pos[r];
+ *   tree:   row_first(r) <= j < base (the committed prefix), or j = base + i where bit i of node r's
+ *           ancestor-or-self mask is set and, with a window W, node i lies inside node r's window
+ *           (depth_i >= depth_r - W + 1: ancestors are ordered by their logical positions). */
+static int visible(const job_t *J, int r, int64_t j)
+{
+    if (J->tree) {
+        const int64_t base = J->tree[0];
+        if (j < 0) return 0;
+        if (j < base) return j >= row_first(J, r);
+        const int64_t i = j - base;
+        if (i >= J->n_live || !((J->tree[1 + r] >> i) & 1)) return 0;
+        return J->window <= 0 || tree_depth(J->tree[1 + i]) >= tree_depth(J->tree[1 + r]) - J->window + 1;
+    }
+    return j >= row_first(J, r) && j <= J->pos[r];
+}
+
+/* Attention of one live (row, head) pair over its whole visible set.  The keys considered are the
+ * contiguous range [first, p]; keys in it that are not visible get no weight. */
 static void one_pair(job_t *J, int r, int h, double *scores)
 {
-    const int64_t p = J->pos[r];
-    const int64_t first = J->window > 0 ? (p - J->window + 1 > 0 ? p - J->window + 1 : 0) : 0;
+    int64_t first = row_first(J, r);
+    if (J->tree && first > J->tree[0]) first = J->tree[0];   /* node slots are judged by visible() alone */
+    const int64_t p = J->pos[r];   /* tree: base + n_nodes - 1, the last slot any node may see */
     const int64_t n = p - first + 1;
     double qd[OR_D];
     for (int d = 0; d < OR_D; ++d)
         qd[d] = widen_bf16(J->q[((int64_t)r * OR_H + h) * OR_D + d]);
 
     for (int64_t i = 0; i < n; ++i) {
+        if (!visible(J, r, first + i)) {
+            scores[i] = -INFINITY;
+            continue;
+        }
         const uint16_t *k = J->kh + (first + i) * OR_D;
         double acc = 0.0;
         for (int d = 0; d < OR_D; ++d)
@@ -104,6 +146,7 @@ static void one_pair(job_t *J, int r, int h, double *scores)
     } else {
         Z = exp(sink - M);
         for (int64_t i = 0; i < n; ++i) {
+            if (scores[i] == -INFINITY) continue;
             const double w = exp(scores[i] - M);
             const uint16_t *v = J->vh + (first + i) * OR_D;
             Z += w;
@@ -128,9 +171,15 @@ static void one_pair(job_t *J, int r, int h, double *scores)
         double m = -INFINITY;
         for (int64_t j = a; j < b; ++j)
             if (scores[j - first] > m) m = scores[j - first];
+        if (m == -INFINITY) {   /* nothing of this split is visible to the row */
+            for (int d = 0; d < OR_D; ++d) po[d] = 0.0;
+            *pl = -INFINITY;
+            continue;
+        }
         double z = 0.0;
         for (int d = 0; d < OR_D; ++d) acc[d] = 0.0;
         for (int64_t j = a; j < b; ++j) {
+            if (scores[j - first] == -INFINITY) continue;
             const double w = exp(scores[j - first] - m);
             const uint16_t *v = J->vh + j * OR_D;
             z += w;
@@ -174,11 +223,48 @@ static void *worker(void *arg)
  *   part_o   [n_splits][n_rows][6][128], part_lse [n_splits][n_rows][6]
  * Returns 0, or -1 on invalid arguments, -2 on allocation failure.
  */
+static int run(const uint16_t *q, const uint16_t *kh, const uint16_t *vh, int64_t ctx, const int32_t *pos,
+               int n_rows, int n_live, const double *sink, double scale, int64_t window, const int32_t *tree,
+               int n_splits, const int64_t *split_a, const int64_t *split_b, double *out, double *lse,
+               double *part_o, double *part_lse, int n_threads);
+
 int oracle_verify_attn(const uint16_t *q, const uint16_t *kh, const uint16_t *vh, int64_t ctx,
                        const int32_t *pos, int n_rows, int n_live, const double *sink,
                        double scale, int64_t window, int n_splits, const int64_t *split_a,
                        const int64_t *split_b, double *out, double *lse, double *part_o,
                        double *part_lse, int n_threads)
+{
+    return run(q, kh, vh, ctx, pos, n_rows, n_live, sink, scale, window, NULL, n_splits, split_a, split_b, out,
+               lse, part_o, part_lse, n_threads);
+}
+
+/*
+ * Tree verification ("Qwen3.8-27B on one RTX 4090", section "More tokens per round: verify trees"): the
+ * draft is a tree of n_nodes nodes verified in one pass under a tree attention mask.  Node i's key and
+ * value sit in slot base + i; node i sees the committed prefix (positions < base; with a window, from
+ * base + depth_i - W + 1 on) and the nodes whose bit is set in its ancestor-or-self mask.
+ *   tree  [1 + n_rows] int32: tree[0] = base, tree[1 + i] = ancestor-or-self mask of node i (i < n_nodes)
+ * Other arguments as oracle_verify_attn; rows past n_nodes are padding.
+ */
+int oracle_verify_attn_tree(const uint16_t *q, const uint16_t *kh, const uint16_t *vh, int64_t ctx,
+                            const int32_t *tree, int n_rows, int n_nodes, const double *sink, double scale,
+                            int64_t window, int n_splits, const int64_t *split_a, const int64_t *split_b,
+                            double *out, double *lse, double *part_o, double *part_lse, int n_threads)
+{
+    if (!tree || n_rows < 1 || n_rows > 64 || n_nodes < 0 || n_nodes > n_rows || n_nodes > 31 || tree[0] < 0)
+        return -1;
+    for (int i = 0; i < n_nodes; ++i)   /* every node sees itself; masks name existing nodes only */
+        if (!((tree[1 + i] >> i) & 1) || (tree[1 + i] >> n_nodes) != 0 || tree[1 + i] < 0) return -1;
+    int32_t last[64];
+    for (int r = 0; r < n_rows; ++r) last[r] = tree[0] + (n_nodes > 0 ? n_nodes - 1 : 0);
+    return run(q, kh, vh, ctx, last, n_rows, n_nodes, sink, scale, window, tree, n_splits, split_a, split_b, out,
+               lse, part_o, part_lse, n_threads);
+}
+
+static int run(const uint16_t *q, const uint16_t *kh, const uint16_t *vh, int64_t ctx, const int32_t *pos,
+               int n_rows, int n_live, const double *sink, double scale, int64_t window, const int32_t *tree,
+               int n_splits, const int64_t *split_a, const int64_t *split_b, double *out, double *lse,
+               double *part_o, double *part_lse, int n_threads)
 {
     if (!q || !kh || !vh || !pos || !out || !lse) return -1;
     if (n_rows < 1 || n_live < 0 || n_live > n_rows || window < 0 || n_splits < 0) return -1;
@@ -200,7 +286,7 @@ int oracle_verify_attn(const uint16_t *q, const uint16_t *kh, const uint16_t *vh
 
     job_t J;
     J.q = q; J.kh = kh; J.vh = vh; J.ctx = ctx; J.pos = pos;
-    J.n_rows = n_rows; J.n_live = n_live; J.sink = sink; J.scale = scale; J.window = window;
+    J.n_rows = n_rows; J.n_live = n_live; J.sink = sink; J.scale = scale; J.window = window; J.tree = tree;
     J.n_splits = n_splits; J.split_a = split_a; J.split_b = split_b;
     J.out = out; J.lse = lse; J.part_o = part_o; J.part_lse = part_lse;
     J.next_pair = 0;

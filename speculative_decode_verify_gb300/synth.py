@@ -13,6 +13,8 @@ head_dim 128, 1K-192K context sweep with synthetic KV, sliding window 4,096 in a
   swa       window 4,096, ring 4,160, context 40,000 (ring wrapped), 7 live rows
   192k      196,608 positions (about 100 MB of K/V), n_live 4..8
   sweep     {1K,4K,16K,32K,64K,128K,192K} x {full, swa} x n_live 4..8
+  trees     16-node draft trees grown best-first ("Qwen3.8-27B on one RTX 4090", section "More
+            tokens per round: verify trees"), verified at the same contexts; node i at slot base + i
 
 Q, K, V ~ N(0, 1) drawn in float32 by a seeded CPU torch generator and rounded to
 bf16; sink ~ N(0, 1) float32; scale = 1/sqrt(128).
@@ -146,6 +148,122 @@ def sweep(idx: int, ctx: int, window: int, n_live: int) -> Workload:
     kind = "swa" if window > 0 else "full"
     return make(f"sweep_{kind}_{ctx}_n{n_live}", 100 + idx, ctx=ctx, n_live=n_live, window=window,
                 slots=slots, n_splits=0)
+
+
+# ----------------------------------------------------------------------------- draft trees
+TREE_NODES = 16
+TREE_TEMPERATURE = 1.25
+
+
+def best_first_tree(g: torch.Generator, n_nodes: int, branch: int = 4, temperature: float = TREE_TEMPERATURE):
+    """Parent array of a synthetic draft tree grown best-first: every node offers `branch` candidate
+    children whose probabilities are a softmax of N(0, 2) logits divided by `temperature`; the candidate
+    with the highest path probability joins the tree next.  parents[0] = -1, parents[i] < i."""
+    parents = [-1]
+    path_logp = [0.0]
+    frontier = []   # (path log-probability, parent)
+
+    def offer(node):
+        logits = torch.randn(branch, generator=g, dtype=torch.float64) * 2.0 / temperature
+        logp = torch.log_softmax(logits, dim=0)
+        for c in range(branch):
+            frontier.append((path_logp[node] + float(logp[c]), node))
+
+    offer(0)
+    while len(parents) < n_nodes:
+        best = max(range(len(frontier)), key=lambda i: frontier[i][0])
+        lp, par = frontier.pop(best)
+        parents.append(par)
+        path_logp.append(lp)
+        offer(len(parents) - 1)
+    return parents
+
+
+def chain_parents(n_nodes: int):
+    return [i - 1 for i in range(n_nodes)]
+
+
+def star_parents(n_nodes: int):
+    return [-1] + [0] * (n_nodes - 1)
+
+
+def ancestor_masks(parents, n_rows: int = TREE_NODES) -> torch.Tensor:
+    """[n_rows] int32: bit k of entry i set iff node k is node i or one of its ancestors (0 past the nodes)."""
+    m = [0] * n_rows
+    for i, par in enumerate(parents):
+        m[i] = (1 << i) | (m[par] if par >= 0 else 0)
+    return torch.tensor(m, dtype=torch.int32)
+
+
+@dataclasses.dataclass
+class TreeWorkload:
+    """One tree verify call: nodes 0..n_nodes-1 at slots base..base+n_nodes-1 (their K/V are the last
+    n_nodes rows of the history); rows n_nodes..n_rows-1 are padding."""
+    name: str
+    seed: int
+    q: torch.Tensor            # [n_rows, 6, 128] bf16
+    k_hist: torch.Tensor       # [base + n_nodes, 128] bf16
+    v_hist: torch.Tensor
+    base: int
+    parents: list
+    masks: torch.Tensor        # [n_rows] int32 ancestor-or-self masks
+    sink: torch.Tensor
+    scale: float
+    window: int
+    slots: int
+    n_splits: int
+
+    @property
+    def n_nodes(self) -> int:
+        return len(self.parents)
+
+    @property
+    def n_rows(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def ctx(self) -> int:
+        return int(self.k_hist.shape[0])
+
+    @property
+    def node_pos(self) -> torch.Tensor:
+        """[n_rows] int32 slots of the nodes (padding rows continue past them), for the append."""
+        return torch.tensor([self.base + i for i in range(self.n_rows)], dtype=torch.int32)
+
+    @property
+    def tree(self) -> torch.Tensor:
+        """[1 + n_rows] int32: base, then the masks (the verify call's tree descriptor)."""
+        return torch.cat([torch.tensor([self.base], dtype=torch.int32), self.masks])
+
+
+def make_tree(name: str, seed: int, base: int, n_nodes: int = TREE_NODES, shape: str = "best_first",
+              window: int = 0, slots: int = 0, n_splits: int = 0, n_rows: int = TREE_NODES) -> TreeWorkload:
+    g = generator(seed)
+    q = normal_bf16((n_rows, Q_HEADS, HEAD_DIM), g)
+    ctx = base + n_nodes
+    k = normal_bf16((ctx, HEAD_DIM), g)
+    v = normal_bf16((ctx, HEAD_DIM), g)
+    sink = torch.randn(Q_HEADS, generator=g, dtype=torch.float32)
+    if shape == "best_first":
+        parents = best_first_tree(g, n_nodes)
+    elif shape == "chain":
+        parents = chain_parents(n_nodes)
+    elif shape == "star":
+        parents = star_parents(n_nodes)
+    else:
+        raise ValueError(shape)
+    if slots <= 0:
+        slots = RING_SLOTS if window > 0 else ctx + 64
+    return TreeWorkload(name=name, seed=seed, q=q, k_hist=k, v_hist=v, base=base, parents=parents,
+                        masks=ancestor_masks(parents, n_rows), sink=sink, scale=SCALE, window=window, slots=slots,
+                        n_splits=n_splits)
+
+
+def tree_192k(n_nodes: int = TREE_NODES, shape: str = "best_first") -> TreeWorkload:
+    """A 16-node tree whose last slot is position 196,607: the same 196,608-position extent as the
+    192K chain workload."""
+    return make_tree(f"tree192k_{shape}_n{n_nodes}", 20 + n_nodes, base=196608 - n_nodes, n_nodes=n_nodes,
+                     shape=shape, slots=196672)
 
 
 def random_partials(seed: int, n_splits: int, n_rows: int, n_live: int, empty_frac: float = 0.1):

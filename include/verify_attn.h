@@ -67,6 +67,7 @@ typedef int va_status;
 #define VA_HEAD_DIM 128       /* head dimension d */
 #define VA_Q_HEADS 6          /* query heads per KV head */
 #define VA_MAX_ROWS 8         /* verify rows per call (one committed token + up to 7 drafts) */
+#define VA_MAX_TREE_NODES 16  /* nodes of a draft tree per verify_attn_tree call */
 #define VA_TILE 64            /* positions per K/V tile and split granule */
 #define VA_MAX_SPLITS 4096    /* largest accepted split count */
 
@@ -76,6 +77,7 @@ typedef int va_status;
 #define VA_DEV_BEYOND_CACHE 4     /* full attention: pos[n_live-1] >= capacity */
 #define VA_DEV_RING_SPAN 8        /* sliding window: pos[n_live-1] - pos[0] > ring_slots - window */
 #define VA_DEV_TIMEOUT 16         /* a kernel gave up on a bounded wait; its outputs are not valid */
+#define VA_DEV_TREE_MASK 32       /* a tree mask lacks its own node's bit or names a node >= n_nodes */
 
 /*
  * kv_ring_append - write the live rows' new K and V into the cache before they are read.
@@ -83,7 +85,7 @@ typedef int va_status;
  * sliding-window ring; verification writes its KV rows before reading them) and "Let correctness
  * checks change the design" (ring of window + one 64-slot tile).
  *   k_new, v_new  device [n_live][128] bf16: the new rows, row r for position pos[r]
- *   n_live        0..8 (0: nothing is written)
+ *   n_live        0..16 (0: nothing is written; up to 16 for the nodes of a draft tree)
  *   k_cache, v_cache  device [slots][128] bf16, updated in place
  *   slots         rows of the cache: the ring size for a sliding-window layer, the capacity for a
  *                 full-attention layer; row r goes to slot pos[r] mod slots
@@ -143,6 +145,44 @@ VA_API va_status verify_attn_swa(const va_bf16 *q, int n_rows, int n_live,
                           int32_t *dev_status, va_stream stream);
 
 /*
+ * verify_attn_tree - split-KV verify attention of a draft TREE under its tree attention mask.
+ * Source: "Qwen3.8-27B on one RTX 4090", section "More tokens per round: verify trees" (the drafts
+ * are grown best-first into a 16-node tree that the target verifies in one pass with a tree
+ * attention mask).  The kernel is the verify_attn_full / verify_attn_swa split kernel with each
+ * node's ancestor mask in place of the causal tail; up to 16 nodes run as two groups of 8 rows.
+ *   q             device [n_rows][6][128] bf16, row i = node i
+ *   n_rows        1..16; n_nodes 0..n_rows (rows past n_nodes are padding: 0 / -inf)
+ *   k_cache, v_cache, slots   window == 0: the full-attention cache [capacity][128] (row j holds
+ *                 position j); window > 0: the sliding-window ring (position p in slot p mod slots;
+ *                 slots a multiple of 64 (else VA_UNSUPPORTED) and >= window + n_nodes - 1 (else
+ *                 VA_RING_TOO_SMALL)).  Node i's K/V sit at position base + i: append them first
+ *                 (kv_ring_append with pos[i] = base + i, same stream).
+ *   window        0 (full attention) or W >= n_nodes (smaller windows: VA_UNSUPPORTED)
+ *   tree          device int32 [1 + n_nodes]: tree[0] = base, the position of node 0 (the committed
+ *                 prefix is positions 0 .. base - 1); tree[1 + i] = ancestor-or-self mask of node i:
+ *                 bit k set iff node k is node i or one of its ancestors
+ *   Node i at depth d_i = popcount(mask_i) - 1 has logical position base + d_i and sees the prefix
+ *   positions max(0, base + d_i - W + 1) .. base - 1 (all of them for full attention) and the
+ *   positions base + k of the nodes k in its mask.  Read extent: [lo, base + n_nodes) with lo = 0
+ *   (full) or max(0, base + min_i d_i - W + 1); splits are dealt over it as for the chain calls.
+ *   scale         as verify_attn_full
+ *   n_splits      1..VA_MAX_SPLITS, or 0 = auto (the ceil(n_rows / 8) node groups share the SMs)
+ *   part_o, part_lse  device float [n_splits][n_rows][6][128] / [n_splits][n_rows][6], as for
+ *                 verify_attn_full; merge them with attn_split_combine (n_rows, n_live = n_nodes)
+ *   splits_used   optional HOST int: the split count launched
+ *   dev_status    optional device int32: VA_DEV_NEGATIVE_POS (base < 0), VA_DEV_BEYOND_CACHE
+ *                 (full: base + n_nodes > capacity), VA_DEV_RING_SPAN (window: the extent is longer
+ *                 than the ring), VA_DEV_TREE_MASK (a mask without its own bit, or naming a node
+ *                 >= n_nodes); the call then writes empty partials
+ * Returns VA_OK, VA_INVALID_ARG, VA_UNSUPPORTED, VA_RING_TOO_SMALL or VA_CUDA_ERROR.
+ */
+VA_API va_status verify_attn_tree(const va_bf16 *q, int n_rows, int n_nodes,
+                           const va_bf16 *k_cache, const va_bf16 *v_cache, int slots, int window,
+                           const int32_t *tree, float scale, int n_splits,
+                           float *part_o, float *part_lse, int *splits_used,
+                           int32_t *dev_status, va_stream stream);
+
+/*
  * attn_split_combine - merge split partials by log-sum-exp and fold in the learned sink.
  * Source: IQuestRT report, "Read only the KV tiles needed by the current positions" (a separate
  * combine kernel issues the partial loads together and keeps four independent FP32
@@ -151,7 +191,7 @@ VA_API va_status verify_attn_swa(const va_bf16 *q, int n_rows, int n_live,
  *   part_o, part_lse  device, as written by verify_attn_full / verify_attn_swa
  *   n_splits      0..VA_MAX_SPLITS
  *   sink          device float [6] (NULL = no sink): logit of a zero-value key, post-scale
- *   n_rows, n_live as for the attention call
+ *   n_rows, n_live as for the attention call (n_rows up to 16 after verify_attn_tree)
  *   out           device [n_rows][6][128] bf16: sum_s exp(lse_s - L) o_s rounded once to bf16
  *                 (nearest, ties to even), L = logsumexp({lse_s} U {sink_h}); padding rows 0
  *   out_lse       optional device float [n_rows][6]: L (-inf for padding rows)

@@ -16,14 +16,14 @@ import threading
 
 __all__ = [
     "VerifyAttnError", "lib", "lib_path", "kv_ring_append", "verify_attn_full", "verify_attn_swa",
-    "attn_split_combine", "verify_attn_full_noalloc", "NOALLOC_MAX_SPLITS", "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string",
-    "HEAD_DIM", "Q_HEADS", "MAX_ROWS", "TILE", "MAX_SPLITS", "EXPORTS",
+    "attn_split_combine", "verify_attn_tree", "verify_attn_full_noalloc", "NOALLOC_MAX_SPLITS", "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string",
+    "HEAD_DIM", "Q_HEADS", "MAX_ROWS", "TILE", "MAX_SPLITS", "MAX_TREE_NODES", "EXPORTS",
     "VA_OK", "VA_INVALID_ARG", "VA_UNSUPPORTED", "VA_RING_TOO_SMALL", "VA_CUDA_ERROR",
 ]
 
-HEAD_DIM, Q_HEADS, MAX_ROWS, TILE, MAX_SPLITS = 128, 6, 8, 64, 4096
+HEAD_DIM, Q_HEADS, MAX_ROWS, TILE, MAX_SPLITS, MAX_TREE_NODES = 128, 6, 8, 64, 4096, 16
 VA_OK, VA_INVALID_ARG, VA_UNSUPPORTED, VA_RING_TOO_SMALL, VA_CUDA_ERROR = 0, 1, 2, 3, 4
-EXPORTS = ("kv_ring_append", "verify_attn_full", "verify_attn_swa", "attn_split_combine",
+EXPORTS = ("kv_ring_append", "verify_attn_full", "verify_attn_swa", "verify_attn_tree", "attn_split_combine",
            "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string",
            "verify_attn_full_noalloc")
 NOALLOC_MAX_SPLITS = 160
@@ -56,10 +56,11 @@ def lib(variant: str = "") -> ctypes.CDLL:
         L.kv_ring_append.argtypes = [p, p, i, p, p, i, p, p, p]
         L.verify_attn_full.argtypes = [p, i, i, p, p, i, p, f, i, p, p, ctypes.POINTER(i), p, p]
         L.verify_attn_swa.argtypes = [p, i, i, p, p, i, i, p, f, i, p, p, ctypes.POINTER(i), p, p]
+        L.verify_attn_tree.argtypes = [p, i, i, p, p, i, i, p, f, i, p, p, ctypes.POINTER(i), p, p]
         L.attn_split_combine.argtypes = [p, p, i, p, i, i, p, p, p]
         L.verify_attn_full_noalloc.argtypes = [p, i, i, p, p, i, p, f, i, p, p, p, ctypes.POINTER(i), p, p]
-        for fn in ("kv_ring_append", "verify_attn_full", "verify_attn_swa", "attn_split_combine",
-                   "verify_attn_full_noalloc"):
+        for fn in ("kv_ring_append", "verify_attn_full", "verify_attn_swa", "verify_attn_tree",
+                   "attn_split_combine", "verify_attn_full_noalloc"):
             getattr(L, fn).restype = i
         L.va_workspace_bytes.argtypes = [i]
         L.va_workspace_bytes.restype = ctypes.c_size_t
@@ -136,6 +137,19 @@ def verify_attn_swa(q, n_live: int, k_ring, v_ring, window: int, pos, scale: flo
                                       _ptr(part_o), _ptr(part_lse), ctypes.byref(used), _ptr(dev_status),
                                       _stream(stream))
     _check("verify_attn_swa", st)
+    return used.value
+
+
+def verify_attn_tree(q, n_nodes: int, k_cache, v_cache, tree, scale: float, part_o, part_lse, window: int = 0,
+                     n_splits: int = 0, dev_status=None, stream=None, variant: str = "") -> int:
+    """Split-KV attention of a draft tree (``tree`` = device int32 [1 + n_nodes]: base, then each node's
+    ancestor-or-self mask) over a full cache (window 0) or a ring; returns the split count."""
+    used = ctypes.c_int(0)
+    st = lib(variant).verify_attn_tree(_ptr(q), int(q.shape[0]), int(n_nodes), _ptr(k_cache), _ptr(v_cache),
+                                       int(k_cache.shape[0]), int(window), _ptr(tree), float(scale), int(n_splits),
+                                       _ptr(part_o), _ptr(part_lse), ctypes.byref(used), _ptr(dev_status),
+                                       _stream(stream))
+    _check("verify_attn_tree", st)
     return used.value
 
 

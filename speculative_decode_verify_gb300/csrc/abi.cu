@@ -73,7 +73,7 @@ extern "C" {
 va_status kv_ring_append(const va_bf16* k_new, const va_bf16* v_new, int n_live, va_bf16* k_cache,
                          va_bf16* v_cache, int slots, const int32_t* pos, int32_t* dev_status,
                          va_stream stream) {
-    if (n_live < 0 || n_live > VA_MAX_ROWS || slots < 1) return VA_INVALID_ARG;
+    if (n_live < 0 || n_live > VA_MAX_TREE_NODES || slots < 1) return VA_INVALID_ARG;
     if (n_live == 0) return VA_OK;
     if (!k_new || !v_new || !k_cache || !v_cache || !pos) return VA_INVALID_ARG;
     if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache)) return VA_INVALID_ARG;
@@ -94,6 +94,7 @@ va_status verify_attn_full(const va_bf16* q, int n_rows, int n_live, const va_bf
     a.part_o = part_o; a.part_lse = part_lse; a.dev_status = dev_status;
     a.scale = scale; a.n_rows = n_rows; a.n_live = n_live; a.slots = capacity; a.window = 0;
     a.n_splits = n_splits;
+    a.tree = nullptr; a.n_groups = 1;
     st = from_cuda(va::launch_attn(a, (cudaStream_t)stream));
     if (st == VA_OK && splits_used) *splits_used = n_splits;
     return st;
@@ -115,14 +116,46 @@ va_status verify_attn_swa(const va_bf16* q, int n_rows, int n_live, const va_bf1
     a.part_o = part_o; a.part_lse = part_lse; a.dev_status = dev_status;
     a.scale = scale; a.n_rows = n_rows; a.n_live = n_live; a.slots = ring_slots; a.window = window;
     a.n_splits = n_splits;
+    a.tree = nullptr; a.n_groups = 1;
     st = from_cuda(va::launch_attn(a, (cudaStream_t)stream));
+    if (st == VA_OK && splits_used) *splits_used = n_splits;
+    return st;
+}
+
+va_status verify_attn_tree(const va_bf16* q, int n_rows, int n_nodes, const va_bf16* k_cache,
+                           const va_bf16* v_cache, int slots, int window, const int32_t* tree, float scale,
+                           int n_splits, float* part_o, float* part_lse, int* splits_used, int32_t* dev_status,
+                           va_stream stream) {
+    if (!q || !k_cache || !v_cache || !tree || !part_o || !part_lse) return VA_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(part_o) || !aligned16(part_lse))
+        return VA_INVALID_ARG;
+    if (n_rows < 1 || n_rows > VA_MAX_TREE_NODES || n_nodes < 0 || n_nodes > n_rows || slots < 1) return VA_INVALID_ARG;
+    if (!std::isfinite(scale) || window < 0 || n_splits < 0 || n_splits > VA_MAX_SPLITS) return VA_INVALID_ARG;
+    const int groups = (n_rows + VA_MAX_ROWS - 1) / VA_MAX_ROWS;
+    if (window > 0) {
+        if (window < n_nodes) return VA_UNSUPPORTED;   // every ancestor must lie inside every window
+        if (slots % VA_TILE != 0) return VA_UNSUPPORTED;
+        if ((long long)slots < (long long)window + (n_nodes > 0 ? n_nodes - 1 : 0)) return VA_RING_TOO_SMALL;
+    }
+    if (n_splits == 0) {
+        // the node groups share the SMs: at most one CTA per SM over all groups
+        const int sms = device_sm_count();
+        const int extent = window > 0 ? window + (n_nodes > 0 ? n_nodes - 1 : 0) : slots;
+        n_splits = va_auto_splits_for(extent, window, (sms > 0 ? sms : 148) / groups);
+    }
+    va::AttnArgs a;
+    a.q = q; a.k = k_cache; a.v = v_cache; a.pos = nullptr; a.tree = tree;
+    a.part_o = part_o; a.part_lse = part_lse; a.dev_status = dev_status;
+    a.scale = scale; a.n_rows = n_rows; a.n_live = n_nodes; a.slots = slots; a.window = window;
+    a.n_splits = n_splits; a.n_groups = groups;
+    va_status st = from_cuda(va::launch_attn(a, (cudaStream_t)stream));
     if (st == VA_OK && splits_used) *splits_used = n_splits;
     return st;
 }
 
 va_status attn_split_combine(const float* part_o, const float* part_lse, int n_splits, const float* sink,
                              int n_rows, int n_live, va_bf16* out, float* out_lse, va_stream stream) {
-    if (!out || n_rows < 1 || n_rows > VA_MAX_ROWS || n_live < 0 || n_live > n_rows) return VA_INVALID_ARG;
+    if (!out || n_rows < 1 || n_rows > VA_MAX_TREE_NODES || n_live < 0 || n_live > n_rows) return VA_INVALID_ARG;
     if (n_splits < 0 || n_splits > VA_MAX_SPLITS) return VA_INVALID_ARG;
     if (n_splits > 0 && (!part_o || !part_lse)) return VA_INVALID_ARG;
     if (!aligned16(out) || (n_splits > 0 && (!aligned16(part_o) || !aligned16(part_lse)))) return VA_INVALID_ARG;

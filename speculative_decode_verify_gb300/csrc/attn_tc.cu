@@ -30,9 +30,14 @@
 //     PV, so that garbage or NaN there cannot reach the accumulator through a zero probability.
 //   * Every wait is bounded (VA_DEV_TIMEOUT); a timed-out CTA drains its own copies and MMAs, frees its
 //     TMEM and returns.
+//   * Draft trees ("Qwen3.8-27B on one RTX 4090", section "More tokens per round: verify trees"): the
+//     same kernel with the node region masked by each node's ancestor bitmask instead of the causal
+//     tail.  Up to 16 nodes run as two groups of 8 rows (grid.y); the two CTAs of a split read the
+//     same tiles at about the same time, so the second read is served by L2.
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <climits>
 #include <cstring>
 #include <mutex>
 
@@ -115,7 +120,11 @@ struct Misc {
     float alpha[kMaxM];
     float inv_l[kMaxM];
     long long row_lo[kMaxRows], row_hi[kMaxRows];
+    long long tree_base;             // tree calls: slot of node 0; chain calls: no node region (LLONG_MAX)
+    unsigned row_anc[kMaxRows];      // ancestor-or-self mask of each row of this CTA's group
     int pos[kMaxRows];
+    int anc[kMaxNodes];              // tree calls: every node's mask
+    int base;
 };
 constexpr uint32_t kSmemBytes = kOffMisc + (uint32_t)sizeof(Misc) + 1024;
 static_assert(kOffQ % 1024 == 0 && kStage % 1024 == 0 && 2 * kPBytes <= kStage, "swizzle atoms need 1 KB alignment");
@@ -182,8 +191,11 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
     Misc& ms = *reinterpret_cast<Misc*>(base + kOffMisc);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x;
-    const int M = a.n_rows * kH;      // matrix rows present in q / the partials
-    const int ML = a.n_live * kH;     // live matrix rows
+    const int group = blockIdx.y;     // rows [8 group, 8 group + 8) of the call
+    const bool is_tree = a.tree != nullptr;
+    const int M = min(kMaxM, a.n_rows * kH - kMaxM * group);             // matrix rows of this group
+    const int n_live_g = max(0, min(kMaxRows, a.n_live - kMaxRows * group));   // live rows of this group
+    const int ML = n_live_g * kH;     // live matrix rows of this group
     if (tid == 0) VA_TRACE_AT(0);
     auto bar = [](const uint64_t& b) { return ptx::smem_u32(&b); };
 
@@ -226,20 +238,38 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
     ptx::griddep_wait();
     if (tid == 0) VA_TRACE_AT(242);
 
-    // the positions: one request per CTA, shared through shared memory
-    if (warp == 0 && lane < a.n_live)
-        ms.pos[lane] = VA_HINT_POS ? ptx::ld_int_policy(a.pos + lane, ptx::policy_evict_last()) : __ldcg(a.pos + lane);
+    // the positions (or the tree): one request per CTA, shared through shared memory
+    if (warp == 0) {
+        if (!is_tree) {
+            if (lane < a.n_live)
+                ms.pos[lane] =
+                    VA_HINT_POS ? ptx::ld_int_policy(a.pos + lane, ptx::policy_evict_last()) : __ldcg(a.pos + lane);
+        } else if (lane <= a.n_live) {
+            const int w = ptx::ld_int_policy(a.tree + lane, ptx::policy_evict_last());
+            if (lane == 0) ms.base = w;
+            else ms.anc[lane - 1] = w;
+        }
+    }
     __syncthreads();
     int row_pos[kMaxRows];
+    int anc[kMaxNodes];
+    Plan P;
+    if (!is_tree) {
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) row_pos[r] = (r < a.n_live) ? ms.pos[r] : 0;
-    const Plan P = make_plan(row_pos, a.n_live, a.window, a.slots, a.n_splits, split);
-    if (P.status && split == 0 && tid == 0 && a.dev_status) atomicOr(a.dev_status, P.status);
+        for (int r = 0; r < kMaxRows; ++r) row_pos[r] = (r < a.n_live) ? ms.pos[r] : 0;
+        P = make_plan(row_pos, a.n_live, a.window, a.slots, a.n_splits, split);
+    } else {
+#pragma unroll
+        for (int i = 0; i < kMaxNodes; ++i) anc[i] = (i < a.n_live) ? ms.anc[i] : 0;
+        P = make_tree_plan(ms.base, anc, a.n_live, a.window, a.slots, a.n_splits, split);
+    }
+    if (P.status && split == 0 && group == 0 && tid == 0 && a.dev_status) atomicOr(a.dev_status, P.status);
     if (tid == 0) VA_TRACE_AT(243);
-    const int n64 = P.status ? 0 : (int)(P.t1 - P.t0);
+    const int n64 = (P.status || n_live_g == 0) ? 0 : (int)(P.t1 - P.t0);
     const int ntiles = (n64 + 1) >> 1;
-    float* part_o = a.part_o + (long long)split * M * kD;
-    float* part_lse = a.part_lse + (long long)split * M;
+    const int M_all = a.n_rows * kH;
+    float* part_o = a.part_o + ((long long)split * M_all + kMaxM * group) * kD;
+    float* part_lse = a.part_lse + (long long)split * M_all + kMaxM * group;
     const long long own_lo = max(P.lo, P.t0 * kTile);
     const long long own_hi = min(P.hi, P.t1 * kTile);
 
@@ -315,29 +345,41 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
             ptx::mbar_arrive_expect_tx(bar(ms.q_full), kQBytes);
             const uint64_t keep = ptx::policy_evict_last();   // every CTA reads the same q
             if (VA_HINT_Q) {
-                ptx::tma_load_2d_hint(base_s + kOffQ, &tmq, 0, 0, bar(ms.q_full), keep);
-                ptx::tma_load_2d_hint(base_s + kOffQ + kQHalf, &tmq, 64, 0, bar(ms.q_full), keep);
+                ptx::tma_load_2d_hint(base_s + kOffQ, &tmq, 0, kMaxM * group, bar(ms.q_full), keep);
+                ptx::tma_load_2d_hint(base_s + kOffQ + kQHalf, &tmq, 64, kMaxM * group, bar(ms.q_full), keep);
             } else {
-                ptx::tma_load_2d(base_s + kOffQ, &tmq, 0, 0, bar(ms.q_full));
-                ptx::tma_load_2d(base_s + kOffQ + kQHalf, &tmq, 64, 0, bar(ms.q_full));
+                ptx::tma_load_2d(base_s + kOffQ, &tmq, 0, kMaxM * group, bar(ms.q_full));
+                ptx::tma_load_2d(base_s + kOffQ + kQHalf, &tmq, 64, kMaxM * group, bar(ms.q_full));
             }
             ms.t_first = ptx::globaltimer_ns();
             for (int j = 0; j < k_first; ++j) load_k(j);
             for (int j = 0; j < v_first; ++j) load_v(j);
         }
         if (tid < kMaxRows) {
+            // row tid of this group: the positions it sees inside this split, [lo, hi), and its mask of
+            // the node region [tree_base, hi)
             long long lo = 0, hi = 0;
+            unsigned m = 0xFFFFFFFFu;
+            if (!is_tree) {
 #pragma unroll
-            for (int r = 0; r < kMaxRows; ++r) {
-                if (r == tid && r < a.n_live) {
-                    const long long p = row_pos[r];
-                    lo = max(a.window > 0 ? max(0LL, p - a.window + 1) : 0LL, own_lo);
-                    hi = min(p + 1, own_hi);
-                    if (hi < lo) hi = lo;
+                for (int r = 0; r < kMaxRows; ++r) {
+                    if (r == tid && r < n_live_g) {
+                        const long long p = row_pos[r];
+                        lo = max(a.window > 0 ? max(0LL, p - a.window + 1) : 0LL, own_lo);
+                        hi = min(p + 1, own_hi);
+                    }
                 }
+            } else if (tid < n_live_g) {
+                m = (unsigned)ms.anc[kMaxRows * group + tid];
+                const long long logical = (long long)ms.base + tree_depth((int)m);   // the node's own position
+                lo = max(a.window > 0 ? max(0LL, logical - a.window + 1) : 0LL, own_lo);
+                hi = min(P.hi, own_hi);
             }
+            if (hi < lo) hi = lo;
             ms.row_lo[tid] = lo;
             ms.row_hi[tid] = hi;
+            ms.row_anc[tid] = m;
+            if (tid == 0) ms.tree_base = is_tree ? (long long)ms.base : LLONG_MAX;
         }
         if (tid < kMaxM) ms.ref[tid] = tid < ML ? kRefInit : INFINITY;   // padding rows never weigh anything
     }
@@ -477,10 +519,12 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
         const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
         const float c = a.scale * 1.4426950408889634f;   // scores in log2 units
         long long all_lo = own_lo, all_hi = own_hi;
-        for (int r = 0; r < a.n_live; ++r) {
+        for (int r = 0; r < n_live_g; ++r) {
             all_lo = max(all_lo, ms.row_lo[r]);
             all_hi = min(all_hi, ms.row_hi[r]);
         }
+        const long long tree_base = ms.tree_base;
+        all_hi = min(all_hi, tree_base);   // the node region of a tree is never interior
         float ref[kCols], l[kCols];
 #pragma unroll
         for (int i = 0; i < kCols; ++i) {
@@ -522,10 +566,13 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
             bool vis[kCols];
             {   // this column half holds verify rows 4 ch .. 4 ch + 3
                 bool rv[kMaxRows / 2];
+                const long long dk = kp - tree_base;   // node index of key kp in a tree's node region
 #pragma unroll
                 for (int k = 0; k < kMaxRows / 2; ++k) {
                     const int r = (kMaxRows / 2) * ch + k;
-                    rv[k] = interior ? (L < nkeys) : ((r < a.n_live) && kp >= ms.row_lo[r] && kp < ms.row_hi[r]);
+                    const bool in_mask = dk < 0 || (dk < 32 && ((ms.row_anc[r] >> (int)dk) & 1u));
+                    rv[k] = interior ? (L < nkeys)
+                                     : ((r < n_live_g) && kp >= ms.row_lo[r] && kp < ms.row_hi[r] && in_mask);
                 }
 #pragma unroll
                 for (int i = 0; i < kCols; ++i) vis[i] = rv[i / kH];
@@ -724,6 +771,7 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int rows, int box_rows)
 }  // namespace tc
 
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
+    if (a.n_groups < 1 || a.n_groups * kMaxRows < a.n_rows || (a.n_groups > 1 && !a.tree)) return cudaErrorInvalidValue;
     CUtensorMap tmq, tmk, tmv, tmk2, tmv2;
     if (!tc::encode_rows_map(&tmq, a.q, a.n_rows * kH, 48) || !tc::encode_rows_map(&tmk, a.k, a.slots, 64) ||
         !tc::encode_rows_map(&tmv, a.v, a.slots, 64) || !tc::encode_rows_map(&tmk2, a.k, a.slots, 128) ||
@@ -733,7 +781,7 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    pdl_config(&cfg, attr, dim3(a.n_splits), dim3(tc::kThreads), tc::kSmemBytes, stream);
+    pdl_config(&cfg, attr, dim3(a.n_splits, a.n_groups), dim3(tc::kThreads), tc::kSmemBytes, stream);
     e = cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel, a, tmq, tmk, tmv, tmk2, tmv2);
     return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -68,6 +68,7 @@ extern "C" VA_API va_status verify_attn_full_noalloc(const va_bf16* q, int n_row
     a.part_o = part_o; a.part_lse = part_lse; a.dev_status = dev_status;
     a.scale = scale; a.n_rows = n_rows; a.n_live = n_live; a.slots = capacity; a.window = 0;
     a.n_splits = n_splits;
+    a.tree = nullptr; a.n_groups = 1;
     if (va::launch_attn(a, (cudaStream_t)stream) != cudaSuccess) return VA_CUDA_ERROR;
     if (va::launch_combine(part_o, part_lse, n_splits, sink, n_rows, n_live, out, out_lse, (cudaStream_t)stream) !=
         cudaSuccess)

@@ -13,18 +13,21 @@ constexpr int kH = VA_Q_HEADS;         // 6
 constexpr int kMaxRows = VA_MAX_ROWS;  // 8
 constexpr int kTile = VA_TILE;         // 64
 constexpr int kMaxM = kH * kMaxRows;   // 48 matrix rows
+constexpr int kMaxNodes = VA_MAX_TREE_NODES;   // 16: two groups of kMaxRows rows
 
 // Arguments of one split-KV attention launch (full attention: window == 0).
 struct AttnArgs {
     const uint16_t* q;       // [n_rows][6][128] bf16
     const uint16_t* k;       // [slots][128] bf16
     const uint16_t* v;       // [slots][128] bf16
-    const int32_t* pos;      // [n_rows]
+    const int32_t* pos;      // [n_rows] (chain calls)
+    const int32_t* tree;     // tree calls: [1 + n_live] base, then ancestor-or-self masks; nullptr for chains
     float* part_o;           // [S][n_rows][6][128]
     float* part_lse;         // [S][n_rows][6]
     int32_t* dev_status;     // optional
     float scale;
     int n_rows, n_live, slots, window, n_splits;
+    int n_groups;            // groups of kMaxRows rows (grid.y); 1 for chain calls
 };
 
 // Extent and split ownership derived on the device from the positions.
@@ -35,6 +38,15 @@ struct Plan {
     long long t0, t1;      // this split's 64-position tiles [t0, t1)
     int status;            // VA_DEV_* bits, 0 if the positions are usable
 };
+
+// Split s of S owns tiles [t_lo + floor(s T / S), t_lo + floor((s + 1) T / S)) of the extent's T tiles.
+__device__ __forceinline__ void deal_tiles(Plan& P, int n_splits, int split) {
+    const long long tlo = P.lo / kTile;
+    const long long thi = (P.hi + kTile - 1) / kTile - 1;
+    const long long T = thi - tlo + 1;
+    P.t0 = tlo + (long long)split * T / n_splits;
+    P.t1 = tlo + (long long)(split + 1) * T / n_splits;
+}
 
 // row_pos[] holds the live rows' positions (entries past n_live are ignored).  Callers load them once
 // per CTA (one request) and share them: every thread of every CTA loading the same eight integers
@@ -62,11 +74,39 @@ __device__ __forceinline__ Plan make_plan(const int (&row_pos)[kMaxRows], int n_
     if (P.status) return P;
     P.hi = (long long)last + 1;
     P.lo = window > 0 ? max(0LL, (long long)p0 - window + 1) : 0LL;
-    const long long tlo = P.lo / kTile;
-    const long long thi = (P.hi + kTile - 1) / kTile - 1;
-    const long long T = thi - tlo + 1;
-    P.t0 = tlo + (long long)split * T / n_splits;
-    P.t1 = tlo + (long long)(split + 1) * T / n_splits;
+    deal_tiles(P, n_splits, split);
+    return P;
+}
+
+// Depth of a tree node: the number of its strict ancestors.
+__device__ __forceinline__ int tree_depth(int mask) { return __popc((unsigned)mask) - 1; }
+
+// Extent and split ownership of a tree call ("Qwen3.8-27B on one RTX 4090", section "More tokens per
+// round: verify trees").  Node i sits at slot base + i and sees the prefix from its window start
+// base + depth_i - window + 1 (0 for full attention) and the nodes of its ancestor-or-self mask.
+// The extent is [lo, base + n_nodes) with lo the earliest window start over the nodes.
+__device__ __forceinline__ Plan make_tree_plan(int base, const int (&anc)[kMaxNodes], int n_nodes, int window,
+                                               int slots, int n_splits, int split) {
+    Plan P;
+    P.lo = P.hi = P.t0 = P.t1 = 0;
+    P.status = 0;
+    if (n_nodes <= 0) return P;
+    if (base < 0) P.status |= VA_DEV_NEGATIVE_POS;
+    int dmin = kMaxNodes;
+#pragma unroll
+    for (int i = 0; i < kMaxNodes; ++i) {
+        if (i >= n_nodes) break;
+        const unsigned m = (unsigned)anc[i];
+        if (!((m >> i) & 1u) || (m >> n_nodes) != 0u) P.status |= VA_DEV_TREE_MASK;
+        dmin = min(dmin, tree_depth((int)m));
+    }
+    const long long hi = (long long)base + n_nodes;
+    if (window == 0 && hi > (long long)slots) P.status |= VA_DEV_BEYOND_CACHE;
+    if (window > 0 && hi - ((long long)base + dmin - window + 1) > (long long)slots) P.status |= VA_DEV_RING_SPAN;
+    if (P.status) return P;
+    P.hi = hi;
+    P.lo = window > 0 ? min((long long)base, max(0LL, (long long)base + dmin - window + 1)) : 0LL;
+    deal_tiles(P, n_splits, split);
     return P;
 }
 

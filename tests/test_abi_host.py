@@ -116,7 +116,7 @@ def test_swa_ring_checks(L):
 
 
 def test_append_and_combine_reject_bad_arguments(L):
-    assert L.kv_ring_append(FAKE, FAKE, 9, FAKE, FAKE, 64, FAKE, None, None) == va.VA_INVALID_ARG
+    assert L.kv_ring_append(FAKE, FAKE, 17, FAKE, FAKE, 64, FAKE, None, None) == va.VA_INVALID_ARG
     assert L.kv_ring_append(FAKE, FAKE, 2, FAKE, FAKE, 0, FAKE, None, None) == va.VA_INVALID_ARG
     assert L.kv_ring_append(None, FAKE, 2, FAKE, FAKE, 64, FAKE, None, None) == va.VA_INVALID_ARG
     assert L.kv_ring_append(None, None, 0, None, None, 64, None, None, None) == va.VA_OK   # nothing to do
@@ -124,6 +124,30 @@ def test_append_and_combine_reject_bad_arguments(L):
     assert L.attn_split_combine(None, FAKE, 4, None, 8, 8, FAKE, None, None) == va.VA_INVALID_ARG
     assert L.attn_split_combine(FAKE, FAKE, 4097, None, 8, 8, FAKE, None, None) == va.VA_INVALID_ARG
     assert L.attn_split_combine(FAKE, FAKE, 4, None, 8, 9, FAKE, None, None) == va.VA_INVALID_ARG
+    assert L.attn_split_combine(FAKE, FAKE, 4, None, 17, 8, FAKE, None, None) == va.VA_INVALID_ARG
+
+
+def _tree(L, **kw):
+    a = dict(q=FAKE, n_rows=16, n_nodes=16, k=FAKE, v=FAKE, slots=4160, W=4096, tree=FAKE, scale=0.088, S=4,
+             po=FAKE, pl=FAKE)
+    a.update(kw)
+    return L.verify_attn_tree(a["q"], a["n_rows"], a["n_nodes"], a["k"], a["v"], a["slots"], a["W"], a["tree"],
+                              a["scale"], a["S"], a["po"], a["pl"], None, None, None)
+
+
+@pytest.mark.parametrize("kw", [dict(q=None), dict(tree=None), dict(k=None), dict(po=None), dict(n_rows=0),
+                                dict(n_rows=17), dict(n_nodes=-1), dict(n_nodes=17), dict(n_rows=8, n_nodes=9),
+                                dict(slots=0), dict(W=-1), dict(S=-1), dict(S=4097),
+                                dict(scale=float("nan")), dict(q=ctypes.c_void_p(0x1008))])
+def test_tree_rejects_bad_arguments(L, kw):
+    assert _tree(L, **kw) == va.VA_INVALID_ARG
+
+
+def test_tree_window_and_ring_checks(L):
+    assert _tree(L, W=15) == va.VA_UNSUPPORTED            # a window shorter than the tree
+    assert _tree(L, slots=4100) == va.VA_UNSUPPORTED      # ring not a multiple of 64
+    assert _tree(L, slots=4096) == va.VA_RING_TOO_SMALL   # needs W + 15 slots
+    assert _tree(L, W=4160 - 14) == va.VA_RING_TOO_SMALL
 
 
 def test_workspace_and_status_strings(L):

@@ -61,6 +61,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the 1K-192K context sweep")
+    ap.add_argument("--no-tree", action="store_true", help="skip the 16-node draft-tree measurement")
     ap.add_argument("--splits", type=int, default=0, help="split count (0 = library policy)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="profiling aid: only the split-attention launches, over --caches rotating caches")
@@ -380,6 +381,74 @@ def ours(args, dist: Dist):
         return {"ctx": ctx, "kind": "swa" if window else "full", "n_live": n, "splits": Ss, "us_per_call": us,
                 "gbs": nbytes / us / 1e3}
 
+    def tree_measure(reps=300):
+        """A 16-node best-first draft tree at the 192K extent (nodes at 196,592..196,607): per call
+        kv_ring_append of the 16 nodes + verify_attn_tree + attn_split_combine, graph-replayed over three
+        rotating caches, and the tree kernel alone back to back."""
+        ts = []
+        for i in range(3):
+            w = synth.make_tree(f"bench_tree{i}", 500 + i, base=CTX - synth.TREE_NODES, slots=CAPACITY)
+            k = torch.full((CAPACITY, 128), synth.BF16_NAN, dtype=torch.int16, device=dev)
+            v = torch.full((CAPACITY, 128), synth.BF16_NAN, dtype=torch.int16, device=dev)
+            k[:w.base] = synth.bits(w.k_hist)[:w.base].to(dev)
+            v[:w.base] = synth.bits(w.v_hist)[:w.base].to(dev)
+            ts.append(dict(w=w, k=k, v=v, q=synth.bits(w.q).to(dev), tree=w.tree.to(dev), pos=w.node_pos.to(dev),
+                           kn=synth.bits(w.k_hist)[w.base:].contiguous().to(dev),
+                           vn=synth.bits(w.v_hist)[w.base:].contiguous().to(dev), sink=w.sink.to(dev),
+                           out=torch.empty(16, 6, 128, dtype=torch.int16, device=dev)))
+        groups = 2
+        St = va.va_auto_splits_for(CAPACITY, 0, torch.cuda.get_device_properties(dev).multi_processor_count // groups)
+        po = torch.empty(St, 16, 6, 128, dtype=torch.float32, device=dev)
+        pl = torch.empty(St, 16, 6, dtype=torch.float32, device=dev)
+
+        def attn(c):
+            w = c["w"]
+            return L.verify_attn_tree(P(c["q"].data_ptr()), 16, w.n_nodes, P(c["k"].data_ptr()), P(c["v"].data_ptr()),
+                                      CAPACITY, 0, P(c["tree"].data_ptr()), ctypes.c_float(w.scale), St,
+                                      P(po.data_ptr()), P(pl.data_ptr()), None, None, sp)
+
+        def one(c):
+            n = c["w"].n_nodes
+            st = L.kv_ring_append(P(c["kn"].data_ptr()), P(c["vn"].data_ptr()), n, P(c["k"].data_ptr()),
+                                  P(c["v"].data_ptr()), CAPACITY, P(c["pos"].data_ptr()), None, sp)
+            st |= attn(c)
+            st |= L.attn_split_combine(P(po.data_ptr()), P(pl.data_ptr()), St, P(c["sink"].data_ptr()), 16, n,
+                                       P(c["out"].data_ptr()), None, sp)
+            if st:
+                raise RuntimeError(f"tree call failed with status {st}")
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                for c in ts:
+                    one(c)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for c in ts:
+                    one(c)
+            g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            us_call = e0.elapsed_time(e1) * 1e3 / (reps * len(ts))
+            e0.record(stream)
+            for _ in range(reps):
+                for c in ts:
+                    if attn(c):
+                        raise RuntimeError("verify_attn_tree failed")
+            e1.record(stream)
+            e1.synchronize()
+            us_attn = e0.elapsed_time(e1) * 1e3 / (reps * len(ts))
+        kv = 512 * CTX
+        call_b = kv + 2 * 16 * 6 * 128 * 2 + 2 * 512 * 16 + 17 * 4
+        attn_b = kv + 16 * 6 * 128 * 2 + 17 * 4
+        return {"workload": "16-node best-first draft tree, nodes at 196,592..196,607 of a 196,608-position "
+                            "full-attention cache (100.7 MB K/V), 3 rotating caches",
+                "n_splits": St, "groups": groups, "us_per_call": us_call, "gbs_call": call_b / us_call / 1e3,
+                "attn_us_per_launch": us_attn, "attn_gbs": attn_b / us_attn / 1e3}
+
     if args.kernel_only:
         # the split-attention kernel alone, back to back over the rotating caches (for ncu captures)
         with torch.cuda.stream(stream):
@@ -483,6 +552,7 @@ def ours(args, dist: Dist):
         dist.barrier()
     clk = clocks.stop()
 
+    tree = None if args.no_tree else tree_measure()
     sweep = []
     if not args.no_sweep:
         for ctx_s in synth.SWEEP_CONTEXTS:
@@ -519,6 +589,7 @@ def ours(args, dist: Dist):
                 "us_per_step": t_e2e / ke * 1e6},
         "gpu_launches": 3 * len(calls) * args.steps,
         "sweep": [{k: (round(v, 2) if isinstance(v, float) else v) for k, v in p.items()} for p in sweep],
+        "tree": tree,
         "clocks": clk,
     }
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:

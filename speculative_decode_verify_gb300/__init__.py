@@ -16,7 +16,9 @@ import threading
 
 __all__ = [
     "VerifyAttnError", "lib", "lib_path", "kv_ring_append", "verify_attn_full", "verify_attn_swa",
-    "attn_split_combine", "verify_attn_tree", "verify_attn_full_noalloc", "NOALLOC_MAX_SPLITS", "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string",
+    "attn_split_combine", "verify_attn_tree", "verify_attn_full_noalloc", "va_sample_workspace_bytes",
+    "va_sample_topk_topp", "va_accept_chain", "va_tree_accept_settle", "SAMPLE_MAX_K", "SAMPLE_TILE",
+    "SAMPLE_MAX_VOCAB", "NOALLOC_MAX_SPLITS", "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string",
     "HEAD_DIM", "Q_HEADS", "MAX_ROWS", "TILE", "MAX_SPLITS", "MAX_TREE_NODES", "EXPORTS",
     "VA_OK", "VA_INVALID_ARG", "VA_UNSUPPORTED", "VA_RING_TOO_SMALL", "VA_CUDA_ERROR",
 ]
@@ -25,8 +27,10 @@ HEAD_DIM, Q_HEADS, MAX_ROWS, TILE, MAX_SPLITS, MAX_TREE_NODES = 128, 6, 8, 64, 4
 VA_OK, VA_INVALID_ARG, VA_UNSUPPORTED, VA_RING_TOO_SMALL, VA_CUDA_ERROR = 0, 1, 2, 3, 4
 EXPORTS = ("kv_ring_append", "verify_attn_full", "verify_attn_swa", "verify_attn_tree", "attn_split_combine",
            "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string",
-           "verify_attn_full_noalloc")
+           "verify_attn_full_noalloc", "va_sample_workspace_bytes", "va_sample_topk_topp", "va_accept_chain",
+           "va_tree_accept_settle")
 NOALLOC_MAX_SPLITS = 160
+SAMPLE_MAX_K, SAMPLE_TILE, SAMPLE_MAX_VOCAB = 32, 8192, 262144
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _lib = {}
@@ -61,6 +65,13 @@ def lib(variant: str = "") -> ctypes.CDLL:
         L.verify_attn_full_noalloc.argtypes = [p, i, i, p, p, i, p, f, i, p, p, p, ctypes.POINTER(i), p, p]
         for fn in ("kv_ring_append", "verify_attn_full", "verify_attn_swa", "verify_attn_tree",
                    "attn_split_combine", "verify_attn_full_noalloc"):
+            getattr(L, fn).restype = i
+        L.va_sample_workspace_bytes.argtypes = [i, i, i]
+        L.va_sample_workspace_bytes.restype = ctypes.c_size_t
+        L.va_sample_topk_topp.argtypes = [p, i, i, i, f, f, p, p, p, p, p, p, ctypes.c_size_t, p]
+        L.va_accept_chain.argtypes = [p, p, p, p, p, p, i, p, p, i, p, p, p, p, p, p, p]
+        L.va_tree_accept_settle.argtypes = [p, p, i, p, i, p, p, p, p, p, p, p, p]
+        for fn in ("va_sample_topk_topp", "va_accept_chain", "va_tree_accept_settle"):
             getattr(L, fn).restype = i
         L.va_workspace_bytes.argtypes = [i]
         L.va_workspace_bytes.restype = ctypes.c_size_t
@@ -173,3 +184,41 @@ def verify_attn_full_noalloc(q, n_live: int, k_cache, v_cache, pos, scale: float
                                                _ptr(dev_status), _stream(stream))
     _check("verify_attn_full_noalloc", st)
     return used.value
+
+
+# ----------------------------------------------------------------------------- after verification
+def va_sample_workspace_bytes(n_rows: int, vocab: int, top_k: int) -> int:
+    return int(lib().va_sample_workspace_bytes(int(n_rows), int(vocab), int(top_k)))
+
+
+def va_sample_topk_topp(logits, top_k: int, top_p: float, temperature: float, u, ids, probs, counts, tokens,
+                        workspace, stream=None, variant: str = "") -> None:
+    """Top-k / temperature / top-p sampling of logits [n_rows, vocab] (float32, device); writes ids/probs
+    [n_rows, top_k], counts and tokens [n_rows].  ``workspace``: a device byte tensor of at least
+    va_sample_workspace_bytes(n_rows, vocab, top_k) bytes."""
+    n_rows, vocab = int(logits.shape[0]), int(logits.shape[1])
+    st = lib(variant).va_sample_topk_topp(_ptr(logits), n_rows, vocab, int(top_k), float(top_p), float(temperature),
+                                          _ptr(u), _ptr(ids), _ptr(probs), _ptr(counts), _ptr(tokens), _ptr(workspace),
+                                          int(workspace.numel() * workspace.element_size()), _stream(stream))
+    _check("va_sample_topk_topp", st)
+
+
+def va_accept_chain(p_ids, p_probs, p_counts, q_ids, q_probs, q_counts, drafts, target_tokens, n_drafts: int,
+                    u_accept, u_replace, pos, n_accepted, out_tokens, next_pos=None, stream=None,
+                    variant: str = "") -> None:
+    """Rejection-sampling acceptance of a chain of n_drafts drafts (all tensors on the device)."""
+    st = lib(variant).va_accept_chain(_ptr(p_ids), _ptr(p_probs), _ptr(p_counts), _ptr(q_ids), _ptr(q_probs),
+                                      _ptr(q_counts), int(p_ids.shape[1]), _ptr(drafts), _ptr(target_tokens),
+                                      int(n_drafts), _ptr(u_accept), _ptr(u_replace), _ptr(pos), _ptr(n_accepted),
+                                      _ptr(out_tokens), _ptr(next_pos), _stream(stream))
+    _check("va_accept_chain", st)
+
+
+def va_tree_accept_settle(k_cache, v_cache, tree, n_nodes: int, node_tokens, target_tokens, path, emitted,
+                          n_accepted, next_pos=None, dev_status=None, stream=None, variant: str = "") -> None:
+    """Accept a draft tree's path and move its K/V to consecutive positions (k/v_cache may be None)."""
+    slots = int(k_cache.shape[0]) if k_cache is not None else 0
+    st = lib(variant).va_tree_accept_settle(_ptr(k_cache), _ptr(v_cache), slots, _ptr(tree), int(n_nodes),
+                                            _ptr(node_tokens), _ptr(target_tokens), _ptr(path), _ptr(emitted),
+                                            _ptr(n_accepted), _ptr(next_pos), _ptr(dev_status), _stream(stream))
+    _check("va_tree_accept_settle", st)

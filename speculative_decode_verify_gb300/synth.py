@@ -266,6 +266,86 @@ def tree_192k(n_nodes: int = TREE_NODES, shape: str = "best_first") -> TreeWorkl
                      shape=shape, slots=196672)
 
 
+# ----------------------------------------------------------------------------- sampling inputs
+VOCAB = 160000
+
+
+def logits(seed: int, n_rows: int, vocab: int = VOCAB, head: int = 40) -> torch.Tensor:
+    """[n_rows, vocab] float32 logits: N(0, 2) everywhere plus a head of `head` tokens per row raised by
+    U(6, 14), so that top-k 20 / top-p 0.95 cut inside a realistic peaked distribution."""
+    g = generator(seed)
+    x = torch.randn(n_rows, vocab, generator=g, dtype=torch.float32) * 2.0
+    for r in range(n_rows):
+        idx = torch.randperm(vocab, generator=g)[:head]
+        x[r, idx] += 6.0 + 8.0 * torch.rand(head, generator=g)
+    return x
+
+
+def uniforms(seed: int, n: int) -> torch.Tensor:
+    """n float32 uniforms in [0, 1)."""
+    return torch.rand(n, generator=generator(seed), dtype=torch.float32)
+
+
+def sparse_distribution(g: torch.Generator, k: int, support, boost=None):
+    """A distribution over k distinct token ids drawn from `support`, probabilities from exp(N(0, 1.5))
+    (optionally raised on `boost` ids), sorted descending.  Returns (ids int32 [k], probs float32 [k])."""
+    support = torch.as_tensor(support)
+    ids = support[torch.randperm(support.numel(), generator=g)[:k]]
+    w = torch.exp(torch.randn(k, generator=g, dtype=torch.float64) * 1.5)
+    if boost is not None:
+        for b in boost:
+            w[ids == int(b)] *= 4.0
+    order = torch.argsort(-w, stable=True)
+    ids, w = ids[order], w[order]
+    return ids.to(torch.int32), (w / w.sum()).to(torch.float32)
+
+
+def chain_round(seed: int, n_drafts: int, k: int = 20, vocab_span: int = 60):
+    """Synthetic inputs of one chain acceptance: per verify row r a target distribution p_r, per draft
+    i a proposal distribution q_i (overlapping p_{i-1}'s ids), the draft token d_i drawn from q_i, the
+    uniforms and the target's own draw per row.  Distributions are padded to k entries (-1 / 0)."""
+    g = generator(seed)
+    rows = n_drafts + 1
+    p_ids = torch.full((rows, k), -1, dtype=torch.int32)
+    p_pr = torch.zeros(rows, k, dtype=torch.float32)
+    q_ids = torch.full((rows, k), -1, dtype=torch.int32)
+    q_pr = torch.zeros(rows, k, dtype=torch.float32)
+    p_cnt = torch.zeros(rows, dtype=torch.int32)
+    q_cnt = torch.zeros(rows, dtype=torch.int32)
+    drafts = torch.zeros(rows, dtype=torch.int32)
+    target = torch.zeros(rows, dtype=torch.int32)
+    drafts[0] = 7
+    for r in range(rows):
+        kp = int(torch.randint(1, k + 1, (1,), generator=g))
+        ids, pr = sparse_distribution(g, kp, torch.arange(vocab_span))
+        p_ids[r, :kp], p_pr[r, :kp], p_cnt[r] = ids, pr, kp
+        target[r] = int(ids[int(torch.multinomial(pr.double(), 1, generator=g))])
+    for i in range(1, rows):
+        kq = int(torch.randint(1, k + 1, (1,), generator=g))
+        ids, pr = sparse_distribution(g, kq, torch.arange(vocab_span), boost=p_ids[i - 1, :2].tolist())
+        q_ids[i, :kq], q_pr[i, :kq], q_cnt[i] = ids, pr, kq
+        drafts[i] = int(ids[int(torch.multinomial(pr.double(), 1, generator=g))])
+    return dict(p_ids=p_ids, p_pr=p_pr, p_cnt=p_cnt, q_ids=q_ids, q_pr=q_pr, q_cnt=q_cnt, drafts=drafts,
+                target=target, u_accept=torch.rand(rows, generator=g), u_replace=torch.rand(1, generator=g),
+                pos=torch.tensor([int(torch.randint(0, 1 << 20, (1,), generator=g))], dtype=torch.int32))
+
+
+def tree_round(seed: int, n_nodes: int = TREE_NODES, follow: float = 0.75, vocab_span: int = 1000):
+    """Synthetic inputs of one tree acceptance: a best-first tree, distinct sibling tokens, and at each
+    node a target token that equals one of its children's tokens with probability `follow`."""
+    g = generator(seed)
+    parents = best_first_tree(g, n_nodes)
+    tokens = torch.randperm(vocab_span, generator=g)[:n_nodes].to(torch.int32)
+    target = torch.zeros(n_nodes, dtype=torch.int32)
+    for v in range(n_nodes):
+        kids = [c for c in range(n_nodes) if parents[c] == v]
+        if kids and float(torch.rand(1, generator=g)) < follow:
+            target[v] = tokens[kids[int(torch.randint(0, len(kids), (1,), generator=g))]]
+        else:
+            target[v] = vocab_span + v   # a token no child carries
+    return parents, tokens, target
+
+
 def random_partials(seed: int, n_splits: int, n_rows: int, n_live: int, empty_frac: float = 0.1):
     """Synthetic split partials for testing the merge on its own: o ~ N(0,1) fp32,
     lse ~ N(0, 3) fp32 with a fraction set to -inf (empty splits), sink ~ N(0, 1)."""

@@ -1,7 +1,7 @@
 """Host-side checks of the C ABI (no GPU needed, no kernel launched).
 
-The library must load, export every function include/verify_attn.h declares, reject bad
-arguments before launching anything, and agree with the shapes the pages state.
+The library must load, export every function include/*.h declares, reject bad arguments before
+launching anything, and agree with the shapes the pages state.
 """
 import ctypes
 import os
@@ -15,6 +15,8 @@ from speculative_decode_verify_gb300 import synth
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "verify_attn.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if h.endswith(".h")]
 
 
 @pytest.fixture(scope="module")
@@ -24,12 +26,14 @@ def L():
 
 
 def _declared():
-    src = open(HEADER).read()
-    return re.findall(r"VA_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+    names = []
+    for h in HEADERS:
+        names += re.findall(r"VA_API\s+[\w\s\*]+?\b(\w+)\s*\(", open(h).read())
+    return names
 
 
 def _defines():
-    src = open(HEADER).read()
+    src = "".join(open(h).read() for h in HEADERS)
     return {k: int(v) for k, v in re.findall(r"#define\s+(VA_\w+)\s+(-?\d+)\b", src)}
 
 
@@ -168,3 +172,41 @@ def test_auto_split_policy(L):
         s_swa = va.va_auto_splits_for(4103, 4096, sm)
         assert s_swa == va.va_auto_splits_for(10 ** 6, 4096, sm)   # a window bounds the work
         assert 1 <= s_swa <= sm
+
+
+# ----------------------------------------------------------------------------- sampling, acceptance, settlement
+def test_sample_workspace_and_argument_checks(L):
+    assert va.va_sample_workspace_bytes(8, 160000, 20) == 8 * 20 * 20 * 8 + 32   # 20 tiles x 20 keys x 8 B + counters
+    assert va.va_sample_workspace_bytes(0, 160000, 20) == 0
+    assert va.va_sample_workspace_bytes(8, 160000, 33) == 0
+    assert va.va_sample_workspace_bytes(8, 262148, 20) == 0
+    assert va.va_sample_workspace_bytes(8, 10, 20) == 0
+    f = ctypes.c_float
+    ok = dict(x=FAKE, n=8, vocab=160000, k=20, p=0.95, T=1.0, u=FAKE, ws=FAKE, wsb=25632)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return L.va_sample_topk_topp(a["x"], a["n"], a["vocab"], a["k"], f(a["p"]), f(a["T"]), a["u"], FAKE, FAKE,
+                                     FAKE, FAKE, a["ws"], a["wsb"], None)
+    for kw in (dict(x=None), dict(u=None), dict(ws=None), dict(wsb=25631), dict(vocab=160002), dict(p=0.0),
+               dict(p=1.5), dict(T=0.0), dict(T=-1.0), dict(k=0), dict(n=65), dict(x=ctypes.c_void_p(0x1004))):
+        assert call(**kw) == va.VA_INVALID_ARG, kw
+
+
+def test_accept_and_settle_argument_checks(L):
+    a = [FAKE] * 6 + [20, FAKE, FAKE, 7, FAKE, FAKE, FAKE, FAKE, FAKE, None, None]
+    bad = list(a)
+    bad[9] = 64                                                    # n_drafts out of range
+    assert L.va_accept_chain(*bad) == va.VA_INVALID_ARG
+    bad = list(a)
+    bad[6] = 33                                                    # k_stride out of range
+    assert L.va_accept_chain(*bad) == va.VA_INVALID_ARG
+    bad = list(a)
+    bad[3] = None                                                  # q needed when there are drafts
+    assert L.va_accept_chain(*bad) == va.VA_INVALID_ARG
+    s = [FAKE, FAKE, 64, FAKE, 16, FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None]
+    for i, v in ((4, 17), (4, 0), (3, None), (2, 0), (1, None), (0, ctypes.c_void_p(0x1008))):
+        bad = list(s)
+        bad[i] = v
+        assert L.va_tree_accept_settle(*bad) == va.VA_INVALID_ARG, (i, v)

@@ -61,10 +61,15 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the 1K-192K context sweep")
-    ap.add_argument("--no-tree", action="store_true", help="skip the 16-node draft-tree measurement")
+    ap.add_argument("--no-tree", action="store_true",
+                    help="skip the draft-tree, sampling, acceptance and settlement measurements")
     ap.add_argument("--splits", type=int, default=0, help="split count (0 = library policy)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="profiling aid: only the split-attention launches, over --caches rotating caches")
+    ap.add_argument("--tree-kernel-only", action="store_true",
+                    help="profiling aid: only verify_attn_tree launches (16-node tree, 192K), over 2 caches")
+    ap.add_argument("--sample-kernel-only", action="store_true",
+                    help="profiling aid: only top-k/top-p sampling launches (8 x 160,000 logits), 2 buffers")
     ap.add_argument("--caches", type=int, default=5, help="distinct 192K caches to rotate (1..5)")
     ap.add_argument("--variant", default="", help="library build variant to load (A/B tuning aid)")
     ap.add_argument("--ctx", type=int, default=CTX, help="context of the --kernel-only runs")
@@ -260,6 +265,8 @@ def ours(args, dist: Dist):
     torch.cuda.set_device(dist.local_rank)
     dev = torch.device("cuda", dist.local_rank)
     stream = torch.cuda.Stream(dev)
+    if args.tree_kernel_only or args.sample_kernel_only:
+        return profiling_loop(args, L, dev, stream)
     S = args.splits or va.va_auto_splits(CTX, 0)
 
     calls = []
@@ -449,6 +456,82 @@ def ours(args, dist: Dist):
                 "n_splits": St, "groups": groups, "us_per_call": us_call, "gbs_call": call_b / us_call / 1e3,
                 "attn_us_per_launch": us_attn, "attn_gbs": attn_b / us_attn / 1e3}
 
+    def post_verify_measure(reps=400):
+        """The calls after verification, each graph-replayed: top-k 20 / top-p 0.95 sampling of 8 rows of
+        160,000 logits (32 rotating logit buffers, 164 MB: read cold), rejection-sampling acceptance of 7
+        drafts, and acceptance + settlement of a 16-node tree in the 192K cache."""
+        res = {}
+        n, vocab = 8, synth.VOCAB
+        xs = [synth.logits(700 + i, n).to(dev) for i in range(32)]
+        u = synth.uniforms(7, n).to(dev)
+        ws = torch.zeros(va.va_sample_workspace_bytes(n, vocab, 20), dtype=torch.uint8, device=dev)
+        ids = torch.empty(n, 20, dtype=torch.int32, device=dev)
+        prb = torch.empty(n, 20, dtype=torch.float32, device=dev)
+        cnt = torch.empty(n, dtype=torch.int32, device=dev)
+        tok = torch.empty(n, dtype=torch.int32, device=dev)
+        wsb = ws.numel()
+
+        def sample(x):
+            st = L.va_sample_topk_topp(P(x.data_ptr()), n, vocab, 20, ctypes.c_float(0.95), ctypes.c_float(1.0),
+                                       P(u.data_ptr()), P(ids.data_ptr()), P(prb.data_ptr()), P(cnt.data_ptr()),
+                                       P(tok.data_ptr()), P(ws.data_ptr()), wsb, sp)
+            if st:
+                raise RuntimeError(f"va_sample_topk_topp failed with status {st}")
+
+        c = {k: v.to(dev) for k, v in synth.chain_round(11, 7).items()}
+        na = torch.empty(1, dtype=torch.int32, device=dev)
+        out = torch.empty(8, dtype=torch.int32, device=dev)
+        nxt = torch.empty(1, dtype=torch.int32, device=dev)
+
+        def accept():
+            st = L.va_accept_chain(*[P(c[k].data_ptr()) for k in ("p_ids", "p_pr", "p_cnt", "q_ids", "q_pr", "q_cnt")],
+                                   20, P(c["drafts"].data_ptr()), P(c["target"].data_ptr()), 7,
+                                   P(c["u_accept"].data_ptr()), P(c["u_replace"].data_ptr()), P(c["pos"].data_ptr()),
+                                   P(na.data_ptr()), P(out.data_ptr()), P(nxt.data_ptr()), sp)
+            if st:
+                raise RuntimeError(f"va_accept_chain failed with status {st}")
+
+        parents, ttok, ttgt = synth.tree_round(12)
+        tree = torch.cat([torch.tensor([CTX - 16], dtype=torch.int32), synth.ancestor_masks(parents)]).to(dev)
+        tk, tt = ttok.to(dev), ttgt.to(dev)
+        path = torch.empty(16, dtype=torch.int32, device=dev)
+        em = torch.empty(16, dtype=torch.int32, device=dev)
+        c0 = calls[0]
+
+        def settle():
+            st = L.va_tree_accept_settle(P(c0["k"].data_ptr()), P(c0["v"].data_ptr()), CAPACITY, P(tree.data_ptr()), 16,
+                                         P(tk.data_ptr()), P(tt.data_ptr()), P(path.data_ptr()), P(em.data_ptr()),
+                                         P(na.data_ptr()), P(nxt.data_ptr()), None, sp)
+            if st:
+                raise RuntimeError(f"va_tree_accept_settle failed with status {st}")
+
+        def graph_time(fns):
+            with torch.cuda.stream(stream):
+                for f in fns:
+                    f()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for f in fns:
+                        f()
+                g.replay()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(max(1, reps // len(fns))):
+                    g.replay()
+                e1.record(stream)
+                e1.synchronize()
+            return e0.elapsed_time(e1) * 1e3 / (max(1, reps // len(fns)) * len(fns))
+
+        us = graph_time([lambda x=x: sample(x) for x in xs])
+        nbytes = n * vocab * 4
+        peak = (measured_peaks() or {}).get("hbm_gbs", 6800.0)
+        res["sample_topk_topp"] = {"rows": n, "vocab": vocab, "top_k": 20, "top_p": 0.95, "us_per_call": us,
+                                   "gbs": nbytes / us / 1e3, "frac_of_hbm_peak": nbytes / us / 1e3 / peak,
+                                   "bound": "latency (5.1 MB per call)"}
+        res["accept_chain"] = {"drafts": 7, "us_per_call": graph_time([accept] * 16)}
+        res["tree_accept_settle"] = {"nodes": 16, "us_per_call": graph_time([settle] * 16)}
+        return res
+
     if args.kernel_only:
         # the split-attention kernel alone, back to back over the rotating caches (for ncu captures)
         with torch.cuda.stream(stream):
@@ -553,6 +636,7 @@ def ours(args, dist: Dist):
     clk = clocks.stop()
 
     tree = None if args.no_tree else tree_measure()
+    post = None if args.no_tree else post_verify_measure()
     sweep = []
     if not args.no_sweep:
         for ctx_s in synth.SWEEP_CONTEXTS:
@@ -590,12 +674,74 @@ def ours(args, dist: Dist):
         "gpu_launches": 3 * len(calls) * args.steps,
         "sweep": [{k: (round(v, 2) if isinstance(v, float) else v) for k, v in p.items()} for p in sweep],
         "tree": tree,
+        "after_verify": post,
         "clocks": clk,
     }
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w8)
     if dist.rank == 0:
         print(json.dumps(line))
+
+
+def profiling_loop(args, L, dev, stream):
+    """Only one kind of launch, back to back (for ncu captures): the 16-node tree verify at 192K over two
+    caches, or the top-k / top-p sampling of 8 x 160,000 logits over two buffers."""
+    import ctypes
+
+    import torch
+
+    import speculative_decode_verify_gb300 as va
+    from speculative_decode_verify_gb300 import synth
+
+    P = ctypes.c_void_p
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    fns = []
+    if args.tree_kernel_only:
+        groups = 2
+        S = va.va_auto_splits_for(CAPACITY, 0, torch.cuda.get_device_properties(dev).multi_processor_count // groups)
+        po = torch.empty(S, 16, 6, 128, dtype=torch.float32, device=dev)
+        pl = torch.empty(S, 16, 6, dtype=torch.float32, device=dev)
+        for i in range(2):
+            w = synth.make_tree(f"prof_tree{i}", 500 + i, base=CTX - synth.TREE_NODES, slots=CAPACITY)
+            k = torch.full((CAPACITY, 128), synth.BF16_NAN, dtype=torch.int16, device=dev)
+            v = torch.full((CAPACITY, 128), synth.BF16_NAN, dtype=torch.int16, device=dev)
+            k[:w.ctx] = synth.bits(w.k_hist).to(dev)
+            v[:w.ctx] = synth.bits(w.v_hist).to(dev)
+            c = dict(q=synth.bits(w.q).to(dev), tree=w.tree.to(dev), k=k, v=v, scale=w.scale, n=w.n_nodes)
+            fns.append(lambda c=c: L.verify_attn_tree(P(c["q"].data_ptr()), 16, c["n"], P(c["k"].data_ptr()),
+                                                      P(c["v"].data_ptr()), CAPACITY, 0, P(c["tree"].data_ptr()),
+                                                      ctypes.c_float(c["scale"]), S, P(po.data_ptr()),
+                                                      P(pl.data_ptr()), None, None, sp))
+        kind, nbytes = "verify_attn_tree", 512 * CTX
+    else:
+        n, vocab = 8, synth.VOCAB
+        ws = torch.zeros(va.va_sample_workspace_bytes(n, vocab, 20), dtype=torch.uint8, device=dev)
+        u = synth.uniforms(7, n).to(dev)
+        outs = [torch.empty(n, 20, dtype=torch.int32, device=dev), torch.empty(n, 20, dtype=torch.float32, device=dev),
+                torch.empty(n, dtype=torch.int32, device=dev), torch.empty(n, dtype=torch.int32, device=dev)]
+        for i in range(2):
+            x = synth.logits(700 + i, n).to(dev)
+            fns.append(lambda x=x: L.va_sample_topk_topp(P(x.data_ptr()), n, vocab, 20, ctypes.c_float(0.95),
+                                                         ctypes.c_float(1.0), P(u.data_ptr()),
+                                                         *[P(t.data_ptr()) for t in outs], P(ws.data_ptr()),
+                                                         ws.numel(), sp))
+        kind, nbytes = "va_sample_topk_topp", 8 * synth.VOCAB * 4
+    with torch.cuda.stream(stream):
+        for _ in range(max(args.warmup, 1)):
+            for f in fns:
+                if f():
+                    raise RuntimeError(f"{kind} failed")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            for f in fns:
+                if f():
+                    raise RuntimeError(f"{kind} failed")
+        e1.record(stream)
+        e1.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / (args.steps * len(fns))
+    print(json.dumps({"kernel_only": kind, "launches": args.steps * len(fns), "us_per_launch": us,
+                      "gbs": nbytes / us / 1e3}))
 
 
 def main():

@@ -64,12 +64,24 @@ typedef struct {
     double scale;
     int64_t window;     /* 0: full attention */
     const int32_t *tree; /* NULL, or tree verify: tree[0] = base slot, tree[1 + r] = ancestor mask of node r */
+    const double *kd, *vd; /* NULL, or the history given as doubles (a decoded quantised cache) */
     int n_splits;
     const int64_t *split_a, *split_b; /* [n_splits] position ranges, may be NULL if n_splits == 0 */
     double *out, *lse, *part_o, *part_lse;
     int next_pair;      /* work counter, guarded by mu */
     pthread_mutex_t mu;
 } job_t;
+
+/* Element d of the key / value at absolute position j: bf16 history widened exactly, or the given doubles. */
+static double key_at(const job_t *J, int64_t j, int d)
+{
+    return J->kd ? J->kd[j * OR_D + d] : widen_bf16(J->kh[j * OR_D + d]);
+}
+
+static double value_at(const job_t *J, int64_t j, int d)
+{
+    return J->vd ? J->vd[j * OR_D + d] : widen_bf16(J->vh[j * OR_D + d]);
+}
 
 /* Depth of a tree node: the number of its strict ancestors (bits of its mask other than its own). */
 static int tree_depth(int32_t mask)
@@ -123,10 +135,9 @@ static void one_pair(job_t *J, int r, int h, double *scores)
             scores[i] = -INFINITY;
             continue;
         }
-        const uint16_t *k = J->kh + (first + i) * OR_D;
         double acc = 0.0;
         for (int d = 0; d < OR_D; ++d)
-            acc += qd[d] * widen_bf16(k[d]);
+            acc += qd[d] * key_at(J, first + i, d);
         scores[i] = J->scale * acc;
     }
 
@@ -148,10 +159,9 @@ static void one_pair(job_t *J, int r, int h, double *scores)
         for (int64_t i = 0; i < n; ++i) {
             if (scores[i] == -INFINITY) continue;
             const double w = exp(scores[i] - M);
-            const uint16_t *v = J->vh + (first + i) * OR_D;
             Z += w;
             for (int d = 0; d < OR_D; ++d)
-                acc[d] += w * widen_bf16(v[d]);
+                acc[d] += w * value_at(J, first + i, d);
         }
         for (int d = 0; d < OR_D; ++d) o[d] = acc[d] / Z;
         J->lse[r * OR_H + h] = M + log(Z);
@@ -181,10 +191,9 @@ static void one_pair(job_t *J, int r, int h, double *scores)
         for (int64_t j = a; j < b; ++j) {
             if (scores[j - first] == -INFINITY) continue;
             const double w = exp(scores[j - first] - m);
-            const uint16_t *v = J->vh + j * OR_D;
             z += w;
             for (int d = 0; d < OR_D; ++d)
-                acc[d] += w * widen_bf16(v[d]);
+                acc[d] += w * value_at(J, j, d);
         }
         /* o_s = sum exp(s_j - lse_s) v_j with lse_s = m + ln z */
         for (int d = 0; d < OR_D; ++d) po[d] = acc[d] / z;
@@ -223,10 +232,10 @@ static void *worker(void *arg)
  *   part_o   [n_splits][n_rows][6][128], part_lse [n_splits][n_rows][6]
  * Returns 0, or -1 on invalid arguments, -2 on allocation failure.
  */
-static int run(const uint16_t *q, const uint16_t *kh, const uint16_t *vh, int64_t ctx, const int32_t *pos,
-               int n_rows, int n_live, const double *sink, double scale, int64_t window, const int32_t *tree,
-               int n_splits, const int64_t *split_a, const int64_t *split_b, double *out, double *lse,
-               double *part_o, double *part_lse, int n_threads);
+static int run(const uint16_t *q, const uint16_t *kh, const uint16_t *vh, const double *kd, const double *vd,
+               int64_t ctx, const int32_t *pos, int n_rows, int n_live, const double *sink, double scale,
+               int64_t window, const int32_t *tree, int n_splits, const int64_t *split_a, const int64_t *split_b,
+               double *out, double *lse, double *part_o, double *part_lse, int n_threads);
 
 int oracle_verify_attn(const uint16_t *q, const uint16_t *kh, const uint16_t *vh, int64_t ctx,
                        const int32_t *pos, int n_rows, int n_live, const double *sink,
@@ -234,8 +243,22 @@ int oracle_verify_attn(const uint16_t *q, const uint16_t *kh, const uint16_t *vh
                        const int64_t *split_b, double *out, double *lse, double *part_o,
                        double *part_lse, int n_threads)
 {
-    return run(q, kh, vh, ctx, pos, n_rows, n_live, sink, scale, window, NULL, n_splits, split_a, split_b, out,
-               lse, part_o, part_lse, n_threads);
+    return run(q, kh, vh, NULL, NULL, ctx, pos, n_rows, n_live, sink, scale, window, NULL, n_splits, split_a,
+               split_b, out, lse, part_o, part_lse, n_threads);
+}
+
+/*
+ * The same attention over a history given as doubles (kd, vd [ctx][128]): the keys and values a
+ * quantised cache decodes to (see oracle/kv_codec.py).  Other arguments as oracle_verify_attn.
+ */
+int oracle_verify_attn_f64kv(const uint16_t *q, const double *kd, const double *vd, int64_t ctx,
+                             const int32_t *pos, int n_rows, int n_live, const double *sink, double scale,
+                             int64_t window, int n_splits, const int64_t *split_a, const int64_t *split_b,
+                             double *out, double *lse, double *part_o, double *part_lse, int n_threads)
+{
+    if (!kd || !vd) return -1;
+    return run(q, NULL, NULL, kd, vd, ctx, pos, n_rows, n_live, sink, scale, window, NULL, n_splits, split_a,
+               split_b, out, lse, part_o, part_lse, n_threads);
 }
 
 /*
@@ -257,16 +280,16 @@ int oracle_verify_attn_tree(const uint16_t *q, const uint16_t *kh, const uint16_
         if (!((tree[1 + i] >> i) & 1) || (tree[1 + i] >> n_nodes) != 0 || tree[1 + i] < 0) return -1;
     int32_t last[64];
     for (int r = 0; r < n_rows; ++r) last[r] = tree[0] + (n_nodes > 0 ? n_nodes - 1 : 0);
-    return run(q, kh, vh, ctx, last, n_rows, n_nodes, sink, scale, window, tree, n_splits, split_a, split_b, out,
-               lse, part_o, part_lse, n_threads);
+    return run(q, kh, vh, NULL, NULL, ctx, last, n_rows, n_nodes, sink, scale, window, tree, n_splits, split_a,
+               split_b, out, lse, part_o, part_lse, n_threads);
 }
 
-static int run(const uint16_t *q, const uint16_t *kh, const uint16_t *vh, int64_t ctx, const int32_t *pos,
-               int n_rows, int n_live, const double *sink, double scale, int64_t window, const int32_t *tree,
-               int n_splits, const int64_t *split_a, const int64_t *split_b, double *out, double *lse,
-               double *part_o, double *part_lse, int n_threads)
+static int run(const uint16_t *q, const uint16_t *kh, const uint16_t *vh, const double *kd, const double *vd,
+               int64_t ctx, const int32_t *pos, int n_rows, int n_live, const double *sink, double scale,
+               int64_t window, const int32_t *tree, int n_splits, const int64_t *split_a, const int64_t *split_b,
+               double *out, double *lse, double *part_o, double *part_lse, int n_threads)
 {
-    if (!q || !kh || !vh || !pos || !out || !lse) return -1;
+    if (!q || (!kh && !kd) || (!vh && !vd) || !pos || !out || !lse) return -1;
     if (n_rows < 1 || n_live < 0 || n_live > n_rows || window < 0 || n_splits < 0) return -1;
     if (n_splits > 0 && (!split_a || !split_b || !part_o || !part_lse)) return -1;
     for (int r = 0; r < n_live; ++r)
@@ -285,7 +308,7 @@ static int run(const uint16_t *q, const uint16_t *kh, const uint16_t *vh, int64_
         }
 
     job_t J;
-    J.q = q; J.kh = kh; J.vh = vh; J.ctx = ctx; J.pos = pos;
+    J.q = q; J.kh = kh; J.vh = vh; J.kd = kd; J.vd = vd; J.ctx = ctx; J.pos = pos;
     J.n_rows = n_rows; J.n_live = n_live; J.sink = sink; J.scale = scale; J.window = window; J.tree = tree;
     J.n_splits = n_splits; J.split_a = split_a; J.split_b = split_b;
     J.out = out; J.lse = lse; J.part_o = part_o; J.part_lse = part_lse;

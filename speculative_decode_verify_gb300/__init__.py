@@ -17,7 +17,8 @@ import threading
 __all__ = [
     "VerifyAttnError", "lib", "lib_path", "kv_ring_append", "verify_attn_full", "verify_attn_swa",
     "attn_split_combine", "verify_attn_tree", "verify_attn_full_noalloc", "va_sample_workspace_bytes",
-    "va_sample_topk_topp", "va_accept_chain", "va_tree_accept_settle", "SAMPLE_MAX_K", "SAMPLE_TILE",
+    "va_sample_topk_topp", "va_accept_chain", "va_tree_accept_settle", "kv_ring_append_q8", "verify_attn_q8",
+    "SAMPLE_MAX_K", "SAMPLE_TILE",
     "SAMPLE_MAX_VOCAB", "NOALLOC_MAX_SPLITS", "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string",
     "HEAD_DIM", "Q_HEADS", "MAX_ROWS", "TILE", "MAX_SPLITS", "MAX_TREE_NODES", "EXPORTS",
     "VA_OK", "VA_INVALID_ARG", "VA_UNSUPPORTED", "VA_RING_TOO_SMALL", "VA_CUDA_ERROR",
@@ -28,7 +29,7 @@ VA_OK, VA_INVALID_ARG, VA_UNSUPPORTED, VA_RING_TOO_SMALL, VA_CUDA_ERROR = 0, 1, 
 EXPORTS = ("kv_ring_append", "verify_attn_full", "verify_attn_swa", "verify_attn_tree", "attn_split_combine",
            "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string",
            "verify_attn_full_noalloc", "va_sample_workspace_bytes", "va_sample_topk_topp", "va_accept_chain",
-           "va_tree_accept_settle")
+           "va_tree_accept_settle", "kv_ring_append_q8", "verify_attn_q8")
 NOALLOC_MAX_SPLITS = 160
 SAMPLE_MAX_K, SAMPLE_TILE, SAMPLE_MAX_VOCAB = 32, 8192, 262144
 
@@ -71,7 +72,10 @@ def lib(variant: str = "") -> ctypes.CDLL:
         L.va_sample_topk_topp.argtypes = [p, i, i, i, f, f, p, p, p, p, p, p, ctypes.c_size_t, p]
         L.va_accept_chain.argtypes = [p, p, p, p, p, p, i, p, p, i, p, p, p, p, p, p, p]
         L.va_tree_accept_settle.argtypes = [p, p, i, p, i, p, p, p, p, p, p, p, p]
-        for fn in ("va_sample_topk_topp", "va_accept_chain", "va_tree_accept_settle"):
+        L.kv_ring_append_q8.argtypes = [p, p, i, p, p, p, p, i, p, p, p]
+        L.verify_attn_q8.argtypes = [p, i, i, p, p, p, p, i, i, p, f, i, p, p, ctypes.POINTER(i), p, p]
+        for fn in ("va_sample_topk_topp", "va_accept_chain", "va_tree_accept_settle", "kv_ring_append_q8",
+                   "verify_attn_q8"):
             getattr(L, fn).restype = i
         L.va_workspace_bytes.argtypes = [i]
         L.va_workspace_bytes.restype = ctypes.c_size_t
@@ -222,3 +226,25 @@ def va_tree_accept_settle(k_cache, v_cache, tree, n_nodes: int, node_tokens, tar
                                             _ptr(node_tokens), _ptr(target_tokens), _ptr(path), _ptr(emitted),
                                             _ptr(n_accepted), _ptr(next_pos), _ptr(dev_status), _stream(stream))
     _check("va_tree_accept_settle", st)
+
+
+# ----------------------------------------------------------------------------- quantised K/V cache
+def kv_ring_append_q8(k_new, v_new, n_live: int, k_codes, v_codes, k_scale, v_scale, pos, dev_status=None,
+                      stream=None, variant: str = "") -> None:
+    """Encode the live rows' K/V ([n_live,128] bf16) into the quantised cache at slot pos[r] mod slots."""
+    st = lib(variant).kv_ring_append_q8(_ptr(k_new), _ptr(v_new), int(n_live), _ptr(k_codes), _ptr(v_codes),
+                                        _ptr(k_scale), _ptr(v_scale), int(k_codes.shape[0]), _ptr(pos),
+                                        _ptr(dev_status), _stream(stream))
+    _check("kv_ring_append_q8", st)
+
+
+def verify_attn_q8(q, n_live: int, k_codes, v_codes, k_scale, v_scale, pos, scale: float, part_o, part_lse,
+                   window: int = 0, n_splits: int = 0, dev_status=None, stream=None, variant: str = "") -> int:
+    """Split-KV verify attention over the quantised cache (window 0: full attention); returns the split count."""
+    used = ctypes.c_int(0)
+    st = lib(variant).verify_attn_q8(_ptr(q), int(q.shape[0]), int(n_live), _ptr(k_codes), _ptr(v_codes),
+                                     _ptr(k_scale), _ptr(v_scale), int(k_codes.shape[0]), int(window), _ptr(pos),
+                                     float(scale), int(n_splits), _ptr(part_o), _ptr(part_lse), ctypes.byref(used),
+                                     _ptr(dev_status), _stream(stream))
+    _check("verify_attn_q8", st)
+    return used.value

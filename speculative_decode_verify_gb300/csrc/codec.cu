@@ -1,0 +1,145 @@
+// The quantised K/V cache ("Qwen3.8-27B on one RTX 4090", section "A cheaper cache and state"): the
+// encoding append (keys rotated by the +-1 Hadamard butterfly and coded E4M3, values coded INT8, one
+// scale per row) and the C ABI of the cache's append and verify attention.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "kv_codec.h"
+#include "tc_ptx.cuh"
+#include "va_internal.cuh"
+
+namespace va {
+
+cudaError_t launch_attn_q8(const AttnArgs& a, const float* k_scale, const float* v_scale, cudaStream_t stream);
+
+namespace codec {
+
+// Two floats to E4M3 codes (round to nearest even, saturating); a zero result is coded +0.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
+    uint32_t b = d;
+    if ((b & 0x007Fu) == 0) b &= 0xFF00u;
+    if ((b & 0x7F00u) == 0) b &= 0x00FFu;
+    return b;
+}
+
+__device__ __forceinline__ float warp_max(float m) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    return m;
+}
+
+// One CTA per live row: warp 0 codes its key, warp 1 its value.  Lane l holds elements 4 l .. 4 l + 3.
+__global__ void __launch_bounds__(64) append_q8_kernel(const uint2* __restrict__ k_new, const uint2* __restrict__ v_new,
+                                                       uint8_t* __restrict__ k_codes, int8_t* __restrict__ v_codes,
+                                                       float* __restrict__ k_scale, float* __restrict__ v_scale, int slots,
+                                                       const int32_t* __restrict__ pos, int32_t* dev_status) {
+    const int r = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    ptx::griddep_launch_dependents();
+    ptx::griddep_wait();
+    const uint2 raw = __ldcg((warp == 0 ? k_new : v_new) + (size_t)r * 32 + lane);
+    const int p = __ldcg(pos + r);
+    if (p < 0) {
+        if (threadIdx.x == 0 && dev_status) atomicOr(dev_status, VA_DEV_NEGATIVE_POS);
+        return;
+    }
+    const size_t slot = (size_t)(p % slots);
+    float x[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u), __uint_as_float(raw.y << 16),
+                  __uint_as_float(raw.y & 0xFFFF0000u)};
+    if (warp == 0) {
+        // k' = H k: butterfly stages of width 1 and 2 inside the lane, then 4 .. 64 across lanes
+        const float t0 = __fadd_rn(x[0], x[1]), t1 = __fsub_rn(x[0], x[1]);
+        const float t2 = __fadd_rn(x[2], x[3]), t3 = __fsub_rn(x[2], x[3]);
+        x[0] = __fadd_rn(t0, t2);
+        x[1] = __fadd_rn(t1, t3);
+        x[2] = __fsub_rn(t0, t2);
+        x[3] = __fsub_rn(t1, t3);
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const bool upper = (lane & m) != 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float o = __shfl_xor_sync(0xffffffffu, x[i], m);
+                x[i] = upper ? __fsub_rn(o, x[i]) : __fadd_rn(x[i], o);
+            }
+        }
+        const float mx = warp_max(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
+        const float s = __fdiv_rn(mx, 448.0f);
+        float q[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) q[i] = s > 0.0f ? __fdiv_rn(x[i], s) : 0.0f;
+        const uint32_t codes = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
+        *reinterpret_cast<uint32_t*>(k_codes + slot * kD + 4 * lane) = codes;
+        if (lane == 0) k_scale[slot] = s;
+    } else {
+        const float mx = warp_max(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
+        const float s = __fdiv_rn(mx, 127.0f);
+        uint32_t codes = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int c = s > 0.0f ? max(-127, min(127, __float2int_rn(__fdiv_rn(x[i], s)))) : 0;
+            codes |= ((uint32_t)c & 0xFFu) << (8 * i);
+        }
+        *reinterpret_cast<uint32_t*>(v_codes + slot * kD + 4 * lane) = codes;
+        if (lane == 0) v_scale[slot] = s;
+    }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace codec
+}  // namespace va
+
+extern "C" {
+
+va_status kv_ring_append_q8(const va_bf16* k_new, const va_bf16* v_new, int n_live, uint8_t* k_codes, int8_t* v_codes,
+                            float* k_scale, float* v_scale, int slots, const int32_t* pos, int32_t* dev_status,
+                            va_stream stream) {
+    using va::codec::aligned16;
+    if (n_live < 0 || n_live > VA_Q8_MAX_APPEND || slots < 1) return VA_INVALID_ARG;
+    if (slots % VA_TILE != 0) return VA_UNSUPPORTED;
+    if (n_live == 0) return VA_OK;
+    if (!k_new || !v_new || !k_codes || !v_codes || !k_scale || !v_scale || !pos) return VA_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scale) ||
+        !aligned16(v_scale))
+        return VA_INVALID_ARG;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    va::pdl_config(&cfg, attr, dim3(n_live), dim3(64), 0, (cudaStream_t)stream);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, va::codec::append_q8_kernel, reinterpret_cast<const uint2*>(k_new),
+                                       reinterpret_cast<const uint2*>(v_new), k_codes, v_codes, k_scale, v_scale, slots,
+                                       pos, dev_status);
+    if (e == cudaSuccess) e = cudaGetLastError();
+    return e == cudaSuccess ? VA_OK : VA_CUDA_ERROR;
+}
+
+va_status verify_attn_q8(const va_bf16* q, int n_rows, int n_live, const uint8_t* k_codes, const int8_t* v_codes,
+                         const float* k_scale, const float* v_scale, int slots, int window, const int32_t* pos,
+                         float scale, int n_splits, float* part_o, float* part_lse, int* splits_used,
+                         int32_t* dev_status, va_stream stream) {
+    using va::codec::aligned16;
+    if (!q || !k_codes || !v_codes || !k_scale || !v_scale || !pos || !part_o || !part_lse) return VA_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scale) || !aligned16(v_scale) ||
+        !aligned16(part_o) || !aligned16(part_lse))
+        return VA_INVALID_ARG;
+    if (n_rows < 1 || n_rows > VA_MAX_ROWS || n_live < 0 || n_live > n_rows || slots < 1) return VA_INVALID_ARG;
+    if (!std::isfinite(scale) || window < 0 || n_splits < 0 || n_splits > VA_MAX_SPLITS) return VA_INVALID_ARG;
+    if (slots % VA_TILE != 0) return VA_UNSUPPORTED;
+    if (window > 0 && (long long)slots < (long long)window + (n_live > 0 ? n_live - 1 : 0)) return VA_RING_TOO_SMALL;
+    if (n_splits == 0) n_splits = va_auto_splits(window > 0 ? window + (n_live > 0 ? n_live - 1 : 0) : slots, window);
+    va::AttnArgs a;
+    a.q = q; a.k = reinterpret_cast<const uint16_t*>(k_codes); a.v = reinterpret_cast<const uint16_t*>(v_codes);
+    a.pos = pos; a.tree = nullptr;   // the byte codes travel in the bf16 pointers of AttnArgs
+    a.part_o = part_o; a.part_lse = part_lse; a.dev_status = dev_status;
+    a.scale = scale; a.n_rows = n_rows; a.n_live = n_live; a.slots = slots; a.window = window;
+    a.n_splits = n_splits; a.n_groups = 1;
+    const cudaError_t e = va::launch_attn_q8(a, k_scale, v_scale, (cudaStream_t)stream);
+    if (e != cudaSuccess) return VA_CUDA_ERROR;
+    if (splits_used) *splits_used = n_splits;
+    return VA_OK;
+}
+
+}  // extern "C"

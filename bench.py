@@ -70,6 +70,8 @@ def parse():
                     help="profiling aid: only verify_attn_tree launches (16-node tree, 192K), over 2 caches")
     ap.add_argument("--sample-kernel-only", action="store_true",
                     help="profiling aid: only top-k/top-p sampling launches (8 x 160,000 logits), 2 buffers")
+    ap.add_argument("--q8-kernel-only", action="store_true",
+                    help="profiling aid: only verify_attn_q8 launches (quantised 192K cache), over 2 caches")
     ap.add_argument("--caches", type=int, default=5, help="distinct 192K caches to rotate (1..5)")
     ap.add_argument("--variant", default="", help="library build variant to load (A/B tuning aid)")
     ap.add_argument("--ctx", type=int, default=CTX, help="context of the --kernel-only runs")
@@ -456,6 +458,89 @@ def ours(args, dist: Dist):
                 "n_splits": St, "groups": groups, "us_per_call": us_call, "gbs_call": call_b / us_call / 1e3,
                 "attn_us_per_launch": us_attn, "attn_gbs": attn_b / us_attn / 1e3}
 
+    def q8_caches(n_caches):
+        """Quantised caches of the 192K workload, encoded on the GPU by kv_ring_append_q8 (one call each)."""
+        out = []
+        for i in range(n_caches):
+            n = 8 - i
+            w = synth.full_192k(n)
+            kc = torch.full((CAPACITY, 128), 0x7F, dtype=torch.uint8, device=dev)
+            vc = torch.zeros(CAPACITY, 128, dtype=torch.int8, device=dev)
+            ks = torch.full((CAPACITY,), float("nan"), device=dev)
+            vs = torch.full((CAPACITY,), float("nan"), device=dev)
+            # the history, encoded by the library (the inputs stay referenced until the copy has run)
+            kh, vh = synth.bits(w.k_hist).to(dev), synth.bits(w.v_hist).to(dev)
+            hpos = torch.arange(CTX - n, dtype=torch.int32, device=dev)
+            st = L.kv_ring_append_q8(P(kh.data_ptr()), P(vh.data_ptr()), CTX - n, P(kc.data_ptr()), P(vc.data_ptr()),
+                                     P(ks.data_ptr()), P(vs.data_ptr()), CAPACITY, P(hpos.data_ptr()), None, sp)
+            if st:
+                raise RuntimeError(f"kv_ring_append_q8 failed with status {st}")
+            stream.synchronize()
+            del kh, vh, hpos
+            idx = w.pos[:n].to(torch.int64)
+            out.append(dict(n=n, w=w, kc=kc, vc=vc, ks=ks, vs=vs, q=synth.bits(w.q).to(dev), pos=w.pos.to(dev),
+                            kn=synth.bits(w.k_hist)[idx].contiguous().to(dev),
+                            vn=synth.bits(w.v_hist)[idx].contiguous().to(dev), sink=w.sink.to(dev),
+                            out=torch.empty(8, 6, 128, dtype=torch.int16, device=dev)))
+        torch.cuda.synchronize(dev)
+        return out
+
+    def q8_measure(reps=300):
+        """The quantised-cache verify at the 192K extent (FP8 keys, INT8 values, 264 B per position): the
+        attention launch alone back to back, and the whole call (encoding append of the live rows +
+        verify_attn_q8 + combine) graph-replayed, over three rotating caches (3 x 52 MB > L2)."""
+        qs = q8_caches(3)
+        po = torch.empty(S, 8, 6, 128, dtype=torch.float32, device=dev)
+        pl = torch.empty(S, 8, 6, dtype=torch.float32, device=dev)
+
+        def attn(c):
+            return L.verify_attn_q8(P(c["q"].data_ptr()), 8, c["n"], P(c["kc"].data_ptr()), P(c["vc"].data_ptr()),
+                                    P(c["ks"].data_ptr()), P(c["vs"].data_ptr()), CAPACITY, 0, P(c["pos"].data_ptr()),
+                                    ctypes.c_float(c["w"].scale), S, P(po.data_ptr()), P(pl.data_ptr()), None, None, sp)
+
+        def one(c):
+            st = L.kv_ring_append_q8(P(c["kn"].data_ptr()), P(c["vn"].data_ptr()), c["n"], P(c["kc"].data_ptr()),
+                                     P(c["vc"].data_ptr()), P(c["ks"].data_ptr()), P(c["vs"].data_ptr()), CAPACITY,
+                                     P(c["pos"].data_ptr()), None, sp)
+            st |= attn(c)
+            st |= L.attn_split_combine(P(po.data_ptr()), P(pl.data_ptr()), S, P(c["sink"].data_ptr()), 8, c["n"],
+                                       P(c["out"].data_ptr()), None, sp)
+            if st:
+                raise RuntimeError(f"quantised verify call failed with status {st}")
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                for c in qs:
+                    one(c)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                for c in qs:
+                    if attn(c):
+                        raise RuntimeError("verify_attn_q8 failed")
+            e1.record(stream)
+            e1.synchronize()
+            us_attn = e0.elapsed_time(e1) * 1e3 / (reps * len(qs))
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for c in qs:
+                    one(c)
+            g.replay()
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            us_call = e0.elapsed_time(e1) * 1e3 / (reps * len(qs))
+        hi = statistics.fmean(int(c["pos"][c["n"] - 1]) + 1 for c in qs)
+        attn_b = 264 * hi + Q_BYTES
+        peak = (measured_peaks() or {}).get("hbm_gbs", 6800.0)
+        return {"workload": "quantised cache (E4M3 keys after a Hadamard rotation, INT8 values, fp32 row scales: "
+                            "264 B per position), 196,608 positions (51.9 MB), 3 rotating caches",
+                "n_splits": S, "attn_us_per_launch": us_attn, "attn_gbs": attn_b / us_attn / 1e3,
+                "attn_frac_of_hbm_peak": attn_b / us_attn / 1e3 / peak, "us_per_call": us_call,
+                "bytes_per_position": 264}
+
     def post_verify_measure(reps=400):
         """The calls after verification, each graph-replayed: top-k 20 / top-p 0.95 sampling of 8 rows of
         160,000 logits (32 rotating logit buffers, 164 MB: read cold), rejection-sampling acceptance of 7
@@ -531,6 +616,33 @@ def ours(args, dist: Dist):
         res["accept_chain"] = {"drafts": 7, "us_per_call": graph_time([accept] * 16)}
         res["tree_accept_settle"] = {"nodes": 16, "us_per_call": graph_time([settle] * 16)}
         return res
+
+    if args.q8_kernel_only:
+        # the quantised-cache split kernel alone, back to back over two caches (for ncu captures)
+        qs = q8_caches(2)
+        po = torch.empty(S, 8, 6, 128, dtype=torch.float32, device=dev)
+        pl = torch.empty(S, 8, 6, dtype=torch.float32, device=dev)
+        with torch.cuda.stream(stream):
+            def attn_q8(c):
+                st = L.verify_attn_q8(P(c["q"].data_ptr()), 8, c["n"], P(c["kc"].data_ptr()), P(c["vc"].data_ptr()),
+                                      P(c["ks"].data_ptr()), P(c["vs"].data_ptr()), CAPACITY, 0, P(c["pos"].data_ptr()),
+                                      ctypes.c_float(c["w"].scale), S, P(po.data_ptr()), P(pl.data_ptr()), None, None, sp)
+                if st:
+                    raise RuntimeError(f"verify_attn_q8 failed with status {st}")
+            for _ in range(max(args.warmup, 1)):
+                for c in qs:
+                    attn_q8(c)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                for c in qs:
+                    attn_q8(c)
+            e1.record(stream)
+            e1.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (args.steps * len(qs))
+        print(json.dumps({"kernel_only": "verify_attn_q8", "launches": args.steps * len(qs), "us_per_launch": us,
+                          "gbs": 264 * CTX / us / 1e3}))
+        return
 
     if args.kernel_only:
         # the split-attention kernel alone, back to back over the rotating caches (for ncu captures)
@@ -636,6 +748,7 @@ def ours(args, dist: Dist):
     clk = clocks.stop()
 
     tree = None if args.no_tree else tree_measure()
+    q8 = None if args.no_tree else q8_measure()
     post = None if args.no_tree else post_verify_measure()
     sweep = []
     if not args.no_sweep:
@@ -674,6 +787,7 @@ def ours(args, dist: Dist):
         "gpu_launches": 3 * len(calls) * args.steps,
         "sweep": [{k: (round(v, 2) if isinstance(v, float) else v) for k, v in p.items()} for p in sweep],
         "tree": tree,
+        "quantised_cache": q8,
         "after_verify": post,
         "clocks": clk,
     }

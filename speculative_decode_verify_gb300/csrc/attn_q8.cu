@@ -232,10 +232,12 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
     ptx::griddep_wait();   // every global access of this kernel comes after this
 
     // q first (two 48-row boxes, 128-byte swizzle, the B operand of the rotation) into the second fp16 V
-    // buffer, which is idle until the second tile is widened.  The K and V tiles are requested by their
-    // producer warps after the block barriers: a thread issuing many bulk copies can stall until the copy
-    // engine accepts them, and no barrier of the whole block should wait for that.
-    if (tid == 32) {
+    // buffer, which is idle until the second tile is widened; by thread 0, which initialised the barrier
+    // (no other thread may use a barrier before a block barrier follows its initialisation).  The K and V
+    // tiles are requested by their producer warps after the block barriers: a thread issuing many bulk
+    // copies can stall until the copy engine accepts them, and no barrier of the whole block should wait
+    // for that.
+    if (tid == 0) {
         const uint64_t keep = ptx::policy_evict_last();
         ptx::mbar_arrive_expect_tx(bar(ms.q_tma), kMaxM * kD * 2);
         ptx::tma_load_2d_hint(base_s + kOffQStage, &tmq, 0, 0, bar(ms.q_tma), keep);

@@ -138,3 +138,82 @@ def test_quantised_attention_stays_near_the_bf16_attention():
                                   w.sink.numpy(), w.scale)
     rel = np.linalg.norm(quant["out"] - exact["out"]) / np.linalg.norm(exact["out"])
     assert rel < 0.05
+
+
+def test_the_key_scale_maps_each_row_maximum_to_the_largest_e4m3_value():
+    w = synth.make("codec", 8, ctx=400, n_live=4)
+    codes, s = C.encode_k(_bits(w.k_hist))
+    dec = np.abs(C.e4m3_decode(codes))
+    assert np.all(dec.max(axis=1) == C.E4M3_MAX)
+    vcodes, _ = C.encode_v(_bits(w.v_hist))
+    assert np.all(np.abs(vcodes.astype(np.int64)).max(axis=1) == 127)
+
+
+def test_an_exactly_representable_cache_reduces_to_the_bf16_oracle():
+    # rotated keys r = a e_i + b e_j with a = +-448 and b a small E4M3 value: k = H r / 128 is exact in bf16,
+    # the float32 butterfly gives r back exactly, the scale is 1 and the codes are exact, so attention over
+    # the decoded cache must equal the bf16-path oracle on the same keys; values are integers with a row
+    # maximum of 127 (scale 1, exact codes)
+    rng = np.random.default_rng(9)
+    ctx, H = 180, hadamard(128).astype(np.float64)
+    r = np.zeros((ctx, 128))
+    i = rng.integers(0, 128, ctx)
+    j = (i + 1 + rng.integers(0, 127, ctx)) % 128
+    r[np.arange(ctx), i] = rng.choice([-448.0, 448.0], ctx)
+    r[np.arange(ctx), j] = rng.choice([-8.0, -4.0, 2.0, 6.0, 12.0], ctx)
+    k = r @ H / 128.0
+    v = rng.integers(-126, 127, (ctx, 128)).astype(np.float64)
+    v[np.arange(ctx), rng.integers(0, 128, ctx)] = 127.0
+    kb, vb = oracle.f64_to_bf16_bits(k), oracle.f64_to_bf16_bits(v)
+    assert np.array_equal(oracle.bf16_bits_to_f64(kb), k) and np.array_equal(oracle.bf16_bits_to_f64(vb), v)
+    kc, ks = C.encode_k(kb)
+    vc, vs = C.encode_v(vb)
+    assert np.all(ks == 1.0) and np.all(vs == 1.0)
+    np.testing.assert_array_equal(C.decode_k(kc, ks), k)
+    np.testing.assert_array_equal(C.decode_v(vc, vs), v)
+    w = synth.make("codec", 10, ctx=ctx, n_live=5)
+    q = _bits(w.q)
+    sink = w.sink.numpy()
+    pos = w.pos.numpy()
+    got = C.verify_attn_decoded(q, C.decode_k(kc, ks), C.decode_v(vc, vs), pos, 5, sink, 0.01, n_splits=2)
+    ref = oracle.verify_attn(q, kb, vb, pos, 5, sink, 0.01)
+    np.testing.assert_allclose(got["out"], ref["out"], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(got["lse"][:5], ref["lse"][:5], rtol=1e-12, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- planted mistakes
+def test_planted_codec_mistakes_fail_the_pins(monkeypatch):
+    """Each plausible mistake in the codec oracle (planted on the CPU) fails at least one pin above."""
+    def no_rotation_on_decode(codes, scales):
+        return C.e4m3_decode(codes) * np.asarray(scales, dtype=np.float64)[:, None]
+
+    def key_scale_by_127(k_bits):
+        k = oracle.bf16_bits_to_f64(k_bits).astype(np.float32)
+        kr = C.fwht_f32(k)
+        s = (np.max(np.abs(kr), axis=-1) / np.float32(127.0)).astype(np.float32)
+        return C.e4m3_encode_bits(np.where(s[:, None] > 0, kr / s[:, None], 0).astype(np.float64)), s
+
+    def int8_truncation(v_bits):
+        v = oracle.bf16_bits_to_f64(v_bits).astype(np.float32)
+        s = (np.max(np.abs(v), axis=-1) / np.float32(127.0)).astype(np.float32)
+        ratio = np.where(s[:, None] > 0, (v / s[:, None]).astype(np.float32), np.float32(0))
+        return np.clip(np.trunc(ratio), -127, 127).astype(np.int8), s
+
+    real_round = C.e4m3_round
+
+    def e4m3_ties_away(x):
+        # round half away from zero instead of half to even
+        x = np.asarray(x, dtype=np.float64)
+        v, code = real_round(x)
+        up, _ = real_round(np.nextafter(np.abs(x), np.inf) * np.sign(x))
+        return np.where(np.abs(up) > np.abs(v), up, v), real_round(np.where(np.abs(up) > np.abs(v), up, v))[1]
+
+    cases = [("decode_k", no_rotation_on_decode, test_keys_decode_within_the_e4m3_bound_and_rotated_identity),
+             ("encode_k", key_scale_by_127, test_the_key_scale_maps_each_row_maximum_to_the_largest_e4m3_value),
+             ("encode_v", int8_truncation, test_int8_values_brute_force_and_error_bound),
+             ("e4m3_round", e4m3_ties_away, test_e4m3_rounding_brute_force)]
+    for name, wrong, pin in cases:
+        with monkeypatch.context() as m:
+            m.setattr(C, name, wrong)
+            with pytest.raises(AssertionError):
+                pin()

@@ -53,9 +53,6 @@ namespace tc {
 #ifndef VA_NV
 #define VA_NV 2
 #endif
-#ifndef VA_ROTATE
-#define VA_ROTATE 0
-#endif
 // Start-up shaping: every CTA asks for its first tiles at the same moment and the DRAM serves all of
 // them interleaved, so tile 0 lands no earlier than the rest and no stage frees up for several us.
 // Requesting tile j of the first ring fill j * VA_STAGGER_NS after tile 0 lets tile 0 land first.
@@ -103,7 +100,10 @@ constexpr int kThreads = 32 * (kSoftWarp0 + kSoftWarps);
 constexpr int kSoftThreads = 32 * kSoftWarps;
 constexpr int kCols = kMaxM / 2;          // matrix rows (accumulator columns) per softmax thread
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS0 = 0, kColS1 = 64, kColO = 128;
+// S^T of two tiles (48 columns each), O^T = P_hi V (columns 128..175) and P_lo V (192..239): the PV
+// product runs with N = 128 over [P_hi | P_lo], and columns 176..191 and 240..255 receive the products
+// of the unused P columns (never read).
+constexpr uint32_t kColS0 = 0, kColS1 = 64, kColO = 128, kColLo = 64;
 constexpr float kThresh = 256.0f;         // a probability may reach 2^8 before the reference is raised
 constexpr float kRefInit = -1.0e30f;      // reference maximum before any visible key
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -121,6 +121,7 @@ struct Misc {
     float inv_l[kMaxM];
     long long row_lo[kMaxRows], row_hi[kMaxRows];
     long long tree_base;             // tree calls: slot of node 0; chain calls: no node region (LLONG_MAX)
+    Plan plan;                       // this split's extent and tiles (derived by warp 0)
     unsigned row_anc[kMaxRows];      // ancestor-or-self mask of each row of this CTA's group
     int pos[kMaxRows];
     int anc[kMaxNodes];              // tree calls: every node's mask
@@ -238,7 +239,10 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
     ptx::griddep_wait();
     if (tid == 0) VA_TRACE_AT(242);
 
-    // the positions (or the tree): one request per CTA, shared through shared memory
+    // the positions (or the tree): one request per CTA; warp 0 derives the plan and shares it through
+    // shared memory (the other warps would only compete with it for issue slots)
+    int row_pos[kMaxRows];
+    Plan P;
     if (warp == 0) {
         if (!is_tree) {
             if (lane < a.n_live)
@@ -249,21 +253,26 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
             if (lane == 0) ms.base = w;
             else ms.anc[lane - 1] = w;
         }
+        __syncwarp();
+        if (!is_tree) {
+#pragma unroll
+            for (int r = 0; r < kMaxRows; ++r) row_pos[r] = (r < a.n_live) ? ms.pos[r] : 0;
+            P = make_plan(row_pos, a.n_live, a.window, a.slots, a.n_splits, split);
+        } else {
+            int anc[kMaxNodes];
+#pragma unroll
+            for (int i = 0; i < kMaxNodes; ++i) anc[i] = (i < a.n_live) ? ms.anc[i] : 0;
+            P = make_tree_plan(ms.base, anc, a.n_live, a.window, a.slots, a.n_splits, split);
+        }
+        if (lane == 0) ms.plan = P;
+        if (P.status && split == 0 && group == 0 && lane == 0 && a.dev_status) atomicOr(a.dev_status, P.status);
     }
     __syncthreads();
-    int row_pos[kMaxRows];
-    int anc[kMaxNodes];
-    Plan P;
+    if (warp != 0) P = ms.plan;
     if (!is_tree) {
 #pragma unroll
         for (int r = 0; r < kMaxRows; ++r) row_pos[r] = (r < a.n_live) ? ms.pos[r] : 0;
-        P = make_plan(row_pos, a.n_live, a.window, a.slots, a.n_splits, split);
-    } else {
-#pragma unroll
-        for (int i = 0; i < kMaxNodes; ++i) anc[i] = (i < a.n_live) ? ms.anc[i] : 0;
-        P = make_tree_plan(ms.base, anc, a.n_live, a.window, a.slots, a.n_splits, split);
     }
-    if (P.status && split == 0 && group == 0 && tid == 0 && a.dev_status) atomicOr(a.dev_status, P.status);
     if (tid == 0) VA_TRACE_AT(243);
     const int n64 = (P.status || n_live_g == 0) ? 0 : (int)(P.t1 - P.t0);
     const int ntiles = (n64 + 1) >> 1;
@@ -273,14 +282,17 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
     const long long own_lo = max(P.lo, P.t0 * kTile);
     const long long own_hi = min(P.hi, P.t1 * kTile);
 
-    // Tile j covers 64-position tiles t = t0 + 2j and, unless it is the split's last odd tile, t + 1.
-    // Its cache rows start at slot(t); the two halves are contiguous unless a ring wraps between them.
-    // (VA_ROTATE: the CTA walks its tiles starting from a split-dependent one.)
-    const int rot = (VA_ROTATE && ntiles > 0) ? (int)((split * 7LL) % ntiles) : 0;
-    auto tile_t = [&](int j) { return P.t0 + 2LL * (VA_ROTATE ? (j + rot) % max(ntiles, 1) : j); };
+    // Tile j covers one or two 64-position tiles from t = tile_t(j).  A split with an odd number of them
+    // takes the single one first: at the start the softmax warps wait for data anyway, whereas a short
+    // last tile would add a whole QK / softmax / PV round after the split's last byte has arrived.
+    // The cache rows of tile j start at slot(t); the two halves are contiguous unless a ring wraps between
+    // them.
+    const bool odd = (n64 & 1) != 0;
+    auto tile_t = [&](int j) { return P.t0 + (odd ? (j > 0 ? 2LL * j - 1 : 0LL) : 2LL * j); };
+    auto tile_halves = [&](int j) { return (odd && j == 0) ? 1 : 2; };
     auto tile_slots = [&](int j, int& slot0, int& slot1, int& halves) {
         const long long t = tile_t(j);
-        halves = (t + 1 < P.t1) ? 2 : 1;
+        halves = tile_halves(j);
         slot0 = (int)((t * kTile) % a.slots);
         slot1 = (int)(((t + 1) * kTile) % a.slots);
     };
@@ -445,7 +457,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, 48, 0, 0);   // A = K, B = Q: both K-major
-            constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, 48, 1, 1);   // A = V^T, B = P^T: MN-major
+            constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, 128, 1, 1);  // A = V^T, B = [P_hi | P_lo]^T: MN-major
             bool ok = ptx::mbar_wait(bar(ms.q_full), 0, abort_flag, kWaitNs);
             // Issue whichever product is ready: QK(qk) once K(qk) has landed and its S buffer is free, and
             // PV(pv) once V(pv) has landed and P(pv) is published.  PV never waits for a later K, so the
@@ -479,15 +491,14 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
                     VA_TRACE_TILE(i, 3);
                     VA_TRACE_TILE(i, 6);
                     ptx::tc_fence_after();
-                    const long long t = tile_t(i);
-                    const int nk = (t + 1 < P.t1) ? 8 : 4;
+                    const int nk = tile_halves(i) == 2 ? 8 : 4;
                     for (int kk = 0; kk < nk; ++kk) {
+                        // one MMA for both parts of P: B columns 0..63 are P_hi (48 used), 64..127 P_lo, one
+                        // 128-byte swizzle atom apart (the leading byte offset), so V is read once
                         const uint64_t adesc = ptx::smem_desc(base_s + kOffV + vs * kStage + kk * 2048, kDHalf, 1024);
                         const uint32_t pbase = base_s + kOffK + ps * kStage + kk * 2048;
-                        ptx::mma_bf16(tmem + kColO, adesc, ptx::smem_desc(pbase + kPhiInStage, 8192, 1024), idesc_pv,
-                                      (i > 0 || kk > 0) ? 1u : 0u);
-                        ptx::mma_bf16(tmem + kColO, adesc, ptx::smem_desc(pbase + kPloInStage, 8192, 1024), idesc_pv,
-                                      1u);
+                        ptx::mma_bf16(tmem + kColO, adesc, ptx::smem_desc(pbase + kPhiInStage, kPloInStage - kPhiInStage, 1024),
+                                      idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
                     }
                     ptx::mma_commit(bar(ms.pv_done));
                     ptx::mma_commit(bar(ms.v_empty[vs]));
@@ -547,7 +558,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
             const long long t = tile_t(j);
-            const int nkeys = (t + 1 < P.t1) ? 128 : 64;
+            const int nkeys = tile_halves(j) == 2 ? 128 : 64;
             const long long kbase = t * kTile;
             const long long kp = kbase + L;
             const int sb = j & 1;
@@ -571,8 +582,8 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
                 for (int k = 0; k < kMaxRows / 2; ++k) {
                     const int r = (kMaxRows / 2) * ch + k;
                     const bool in_mask = dk < 0 || (dk < 32 && ((ms.row_anc[r] >> (int)dk) & 1u));
-                    rv[k] = interior ? (L < nkeys)
-                                     : ((r < n_live_g) && kp >= ms.row_lo[r] && kp < ms.row_hi[r] && in_mask);
+                    rv[k] = (L < nkeys) &&
+                            (interior || ((r < n_live_g) && kp >= ms.row_lo[r] && kp < ms.row_hi[r] && in_mask));
                 }
 #pragma unroll
                 for (int i = 0; i < kCols; ++i) vis[i] = rv[i / kH];
@@ -637,12 +648,16 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
                 }
                 if (j > 0) {
                     ptx::tc_fence_after();
-                    float o[kCols];
-                    ptx::tmem_ld24_wait(tl + kColO + n0, o);
 #pragma unroll
-                    for (int i = 0; i < kCols; ++i) o[i] *= ms.alpha[n0 + i];
-                    ptx::tmem_st16(tl + kColO + n0, o);
-                    ptx::tmem_st8(tl + kColO + n0 + 16, o + 16);
+                    for (int part = 0; part < 2; ++part) {   // the accumulators of P_hi V and P_lo V
+                        const uint32_t col = tl + kColO + kColLo * part + n0;
+                        float o[kCols];
+                        ptx::tmem_ld24_wait(col, o);
+#pragma unroll
+                        for (int i = 0; i < kCols; ++i) o[i] *= ms.alpha[n0 + i];
+                        ptx::tmem_st16(col, o);
+                        ptx::tmem_st8(col + 16, o + 16);
+                    }
                     ptx::tmem_wait_st();
                 }
             }
@@ -709,12 +724,13 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
         ptx::named_bar_sync(1, kSoftThreads);
         if (!ptx::mbar_wait(bar(ms.o_ready), 0, abort_flag, kWaitNs)) ok = false;
         ptx::tc_fence_after();
-        float o[kCols];
+        float o[kCols], o_lo[kCols];
         ptx::tmem_ld24_wait(tl + kColO + n0, o);
+        ptx::tmem_ld24_wait(tl + kColO + kColLo + n0, o_lo);
 #pragma unroll
         for (int i = 0; i < kCols; ++i) {
             const int n = n0 + i;
-            if (n < M) part_o[n * kD + L] = o[i] * ms.inv_l[n];
+            if (n < M) part_o[n * kD + L] = (o[i] + o_lo[i]) * ms.inv_l[n];
         }
         if (ch == 0 && L < M) {
             const float lt = ms.alpha[L];

@@ -234,6 +234,38 @@ VA_API const char *va_status_string(va_status status);
  *   va_auto_splits(capacity, 0); a count above VA_NOALLOC_MAX_SPLITS returns VA_INVALID_ARG.
  *   Allocates and frees nothing.  Returns VA_OK, VA_INVALID_ARG or VA_CUDA_ERROR.
  */
+/*
+ * verify_attn_step - one whole verify call: the append of the live rows, the split attention of a
+ * full-attention or sliding-window layer and the combine with the sink, in two launches instead of the
+ * three of kv_ring_append + verify_attn_full / verify_attn_swa + attn_split_combine (the append runs
+ * inside the attention launch).  It computes exactly what those three calls compute.
+ * Source: IQuestRT report, "Read only the KV tiles needed by the current positions" (append before read,
+ * split-KV partials, separate combine) and "Expose more parallelism in attention" (LSE merge, sink
+ * correction, bf16 rounding once).
+ * The split that owns a live row's position writes that row to its slot before it loads the row's tile;
+ * no other split reads it (in a ring, a stale row of the same slot lies below every window).
+ *   q, n_rows, n_live, pos, scale   as verify_attn_full
+ *   k_new, v_new  device [n_live][128] bf16 (may be NULL when n_live == 0), as kv_ring_append
+ *   k_cache, v_cache, slots, window  window == 0: the full-attention cache, slots = capacity (row j holds
+ *                 position j); window >= 1: the ring of a sliding-window layer, as verify_attn_swa
+ *                 (slots a multiple of 64 (else VA_UNSUPPORTED), >= window + n_live - 1 (else
+ *                 VA_RING_TOO_SMALL)).  Updated in place.
+ *   sink          device float [6] or NULL, as attn_split_combine
+ *   n_splits      1..VA_MAX_SPLITS, or 0 = auto (as verify_attn_full / verify_attn_swa)
+ *   workspace     device float, 16-byte aligned, va_workspace_bytes(n_splits) bytes: part_o then
+ *                 part_lse (at n_splits * 8 * 6 * 128 floats), laid out as verify_attn_full's partials
+ *                 for n_rows rows; they stay there after the call
+ *   out, out_lse  as attn_split_combine (n_rows, n_live)
+ *   splits_used   optional HOST int: the split count launched
+ *   dev_status    optional device int32: the bits of verify_attn_full / verify_attn_swa
+ * Returns VA_OK, VA_INVALID_ARG, VA_UNSUPPORTED, VA_RING_TOO_SMALL or VA_CUDA_ERROR.
+ */
+VA_API va_status verify_attn_step(const va_bf16 *q, const va_bf16 *k_new, const va_bf16 *v_new,
+                                  int n_rows, int n_live, va_bf16 *k_cache, va_bf16 *v_cache, int slots,
+                                  int window, const int32_t *pos, const float *sink, float scale,
+                                  int n_splits, float *workspace, va_bf16 *out, float *out_lse,
+                                  int *splits_used, int32_t *dev_status, va_stream stream);
+
 #define VA_NOALLOC_MAX_SPLITS 160
 VA_API va_status verify_attn_full_noalloc(const va_bf16 *q, int n_rows, int n_live,
                                           const va_bf16 *k_cache, const va_bf16 *v_cache, int capacity,

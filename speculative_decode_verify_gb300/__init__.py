@@ -18,7 +18,7 @@ __all__ = [
     "VerifyAttnError", "lib", "lib_path", "kv_ring_append", "verify_attn_full", "verify_attn_swa",
     "attn_split_combine", "verify_attn_tree", "verify_attn_full_noalloc", "va_sample_workspace_bytes",
     "va_sample_topk_topp", "va_accept_chain", "va_tree_accept_settle", "kv_ring_append_q8", "verify_attn_q8",
-    "SAMPLE_MAX_K", "SAMPLE_TILE",
+    "verify_attn_step", "SAMPLE_MAX_K", "SAMPLE_TILE",
     "SAMPLE_MAX_VOCAB", "NOALLOC_MAX_SPLITS", "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string",
     "HEAD_DIM", "Q_HEADS", "MAX_ROWS", "TILE", "MAX_SPLITS", "MAX_TREE_NODES", "EXPORTS",
     "VA_OK", "VA_INVALID_ARG", "VA_UNSUPPORTED", "VA_RING_TOO_SMALL", "VA_CUDA_ERROR",
@@ -29,7 +29,7 @@ VA_OK, VA_INVALID_ARG, VA_UNSUPPORTED, VA_RING_TOO_SMALL, VA_CUDA_ERROR = 0, 1, 
 EXPORTS = ("kv_ring_append", "verify_attn_full", "verify_attn_swa", "verify_attn_tree", "attn_split_combine",
            "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string",
            "verify_attn_full_noalloc", "va_sample_workspace_bytes", "va_sample_topk_topp", "va_accept_chain",
-           "va_tree_accept_settle", "kv_ring_append_q8", "verify_attn_q8")
+           "va_tree_accept_settle", "kv_ring_append_q8", "verify_attn_q8", "verify_attn_step")
 NOALLOC_MAX_SPLITS = 160
 SAMPLE_MAX_K, SAMPLE_TILE, SAMPLE_MAX_VOCAB = 32, 8192, 262144
 
@@ -77,6 +77,8 @@ def lib(variant: str = "") -> ctypes.CDLL:
         for fn in ("va_sample_topk_topp", "va_accept_chain", "va_tree_accept_settle", "kv_ring_append_q8",
                    "verify_attn_q8"):
             getattr(L, fn).restype = i
+        L.verify_attn_step.argtypes = [p, p, p, i, i, p, p, i, i, p, p, f, i, p, p, p, ctypes.POINTER(i), p, p]
+        L.verify_attn_step.restype = i
         L.va_workspace_bytes.argtypes = [i]
         L.va_workspace_bytes.restype = ctypes.c_size_t
         L.va_auto_splits.argtypes = [i, i]
@@ -113,6 +115,20 @@ def va_status_string(status: int) -> str:
 
 def va_workspace_bytes(n_splits: int) -> int:
     return int(lib().va_workspace_bytes(int(n_splits)))
+
+
+def verify_attn_step(q, k_new, v_new, n_live: int, k_cache, v_cache, pos, scale: float, sink, workspace, out,
+                     out_lse=None, window: int = 0, n_splits: int = 0, dev_status=None, stream=None,
+                     variant: str = "") -> int:
+    """One whole verify call (append + split attention + combine, two launches); returns the split count.
+    workspace: float32 device tensor of at least va_workspace_bytes(n_splits) bytes (the partials)."""
+    used = ctypes.c_int(0)
+    st = lib(variant).verify_attn_step(_ptr(q), _ptr(k_new), _ptr(v_new), int(q.shape[0]), int(n_live),
+                                       _ptr(k_cache), _ptr(v_cache), int(k_cache.shape[0]), int(window), _ptr(pos),
+                                       _ptr(sink), float(scale), int(n_splits), _ptr(workspace), _ptr(out),
+                                       _ptr(out_lse), ctypes.byref(used), _ptr(dev_status), _stream(stream))
+    _check("verify_attn_step", st)
+    return used.value
 
 
 def va_auto_splits(extent_hint: int, window: int = 0) -> int:

@@ -163,6 +163,43 @@ va_status attn_split_combine(const float* part_o, const float* part_lse, int n_s
                                         (cudaStream_t)stream));
 }
 
+va_status verify_attn_step(const va_bf16* q, const va_bf16* k_new, const va_bf16* v_new, int n_rows, int n_live,
+                           va_bf16* k_cache, va_bf16* v_cache, int slots, int window, const int32_t* pos,
+                           const float* sink, float scale, int n_splits, float* workspace, va_bf16* out,
+                           float* out_lse, int* splits_used, int32_t* dev_status, va_stream stream) {
+    if (!out || !aligned16(out)) return VA_INVALID_ARG;
+    if (n_live > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))) return VA_INVALID_ARG;
+    if (window < 0 || n_splits < 0 || n_splits > VA_MAX_SPLITS || !workspace) return VA_INVALID_ARG;
+    if (n_splits == 0)
+        n_splits = window > 0 ? va_auto_splits(window + (n_live > 0 ? n_live - 1 : 0), window)
+                              : va_auto_splits(slots, 0);
+    float* part_o = workspace;
+    float* part_lse = workspace + (size_t)n_splits * VA_MAX_ROWS * VA_Q_HEADS * VA_HEAD_DIM;
+    va_status st = check_attn_common(q, n_rows, n_live, k_cache, v_cache, slots, pos, scale, n_splits, part_o,
+                                     part_lse);
+    if (st != VA_OK) return st;
+    if (window > 0) {
+        if (slots % VA_TILE != 0) return VA_UNSUPPORTED;
+        if ((long long)slots < (long long)window + (n_live > 0 ? n_live - 1 : 0)) return VA_RING_TOO_SMALL;
+    }
+    va::AttnArgs a;
+    a.q = q; a.k = k_cache; a.v = v_cache; a.pos = pos;
+    a.part_o = part_o; a.part_lse = part_lse; a.dev_status = dev_status;
+    a.scale = scale; a.n_rows = n_rows; a.n_live = n_live; a.slots = slots; a.window = window;
+    a.n_splits = n_splits;
+    a.tree = nullptr; a.n_groups = 1;
+    if (n_live > 0) {
+        a.k_new = k_new;
+        a.v_new = v_new;
+    }
+    st = from_cuda(va::launch_attn(a, (cudaStream_t)stream));
+    if (st != VA_OK) return st;
+    st = from_cuda(va::launch_combine(part_o, part_lse, n_splits, sink, n_rows, n_live, out, out_lse,
+                                      (cudaStream_t)stream));
+    if (st == VA_OK && splits_used) *splits_used = n_splits;
+    return st;
+}
+
 size_t va_workspace_bytes(int n_splits) {
     if (n_splits < 1 || n_splits > VA_MAX_SPLITS) return 0;
     return sizeof(float) * (size_t)n_splits * VA_MAX_ROWS * VA_Q_HEADS * (VA_HEAD_DIM + 1);

@@ -111,6 +111,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 struct Misc {
     uint64_t k_full[kNK], k_empty[kNK], v_full[kNV], v_empty[kNV];
     uint64_t q_full, s_full[2], s_free[2], p_full[2], pv_done, o_ready, drain;
+    uint64_t app_done;               // verify_attn_step: this split's share of the append is written
     uint32_t tmem_base;
     int abort;
     int vote[2][kSoftWarps];
@@ -181,6 +182,9 @@ __device__ unsigned long long* g_trace = nullptr;
 #define VA_TRACE_TILE(j, k) do { } while (0)
 #endif
 
+// kAppend: the verify_attn_step instantiation, which writes the live rows itself (a.k_new / a.v_new);
+// the instantiation without it carries none of that code.
+template <bool kAppend>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmk2,
@@ -220,6 +224,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
         ptx::mbar_init(bar(ms.pv_done), 1);
         ptx::mbar_init(bar(ms.o_ready), 1);
         ptx::mbar_init(bar(ms.drain), 1);
+        if (kAppend) ptx::mbar_init(bar(ms.app_done), 1);
         ms.abort = 0;
         ptx::mbar_init_fence();
         VA_TRACE_AT(240);
@@ -340,10 +345,21 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
         load_tile(&tmv, &tmv2, base_s + kOffV + (uint32_t)(j % kNV) * kStage, ms.v_full[j % kNV], j);
         if (kPrefetch > 0 && j >= kNV && j + kPrefetch < ntiles) prefetch_tile(&tmv, &tmv2, j + kPrefetch);
     };
+    // verify_attn_step: a tile holding a live row's position is loaded only after the MMA warp, which
+    // appends this split's live rows, has written them (app_done).  Positions are increasing, so the live
+    // rows are the positions [pos[0], hi).
+    constexpr bool step = kAppend;
+    auto tile_has_new = [&](int j) {
+        if (!step) return false;
+        const long long t = tile_t(j);
+        return (long long)row_pos[0] < (t + tile_halves(j)) * kTile && P.hi > t * kTile;
+    };
     // Initial fill: with VA_STAGGER_NS, only tile 0 is requested at once and the producers request
-    // tile j of the first ring fill j * VA_STAGGER_NS after it.
-    const int k_first = VA_STAGGER_NS ? min(1, ntiles) : min(kNK, ntiles);
-    const int v_first = VA_STAGGER_NS ? min(1, ntiles) : min(kNV, ntiles);
+    // tile j of the first ring fill j * VA_STAGGER_NS after it.  (A tile 0 that waits for the append is
+    // requested by the producers.)
+    const bool defer0 = ntiles > 0 && tile_has_new(0);
+    const int k_first = defer0 ? 0 : VA_STAGGER_NS ? min(1, ntiles) : min(kNK, ntiles);
+    const int v_first = defer0 ? 0 : VA_STAGGER_NS ? min(1, ntiles) : min(kNV, ntiles);
     auto stagger = [&](int j) {
         if (VA_STAGGER_NS == 0) return;
         const unsigned long long due = ms.t_first + (unsigned long long)j * VA_STAGGER_NS;
@@ -423,7 +439,8 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
             int issued = k_first;
             for (int j = k_first; j < ntiles; ++j) {
                 if (j < kNK) stagger(j);
-                if (!ptx::mbar_wait(bar(ms.k_empty[j % kNK]), ((j / kNK) & 1) ^ 1, abort_flag, kWaitNs)) {
+                if ((tile_has_new(j) && !ptx::mbar_wait(bar(ms.app_done), 0, abort_flag, kWaitNs)) ||
+                    !ptx::mbar_wait(bar(ms.k_empty[j % kNK]), ((j / kNK) & 1) ^ 1, abort_flag, kWaitNs)) {
                     fail();
                     break;
                 }
@@ -442,7 +459,8 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
             int issued = v_first;
             for (int j = v_first; j < ntiles; ++j) {
                 if (j < kNV) stagger(j);
-                if (!ptx::mbar_wait(bar(ms.v_empty[j % kNV]), ((j / kNV) & 1) ^ 1, abort_flag, kWaitNs)) {
+                if ((tile_has_new(j) && !ptx::mbar_wait(bar(ms.app_done), 0, abort_flag, kWaitNs)) ||
+                    !ptx::mbar_wait(bar(ms.v_empty[j % kNV]), ((j / kNV) & 1) ^ 1, abort_flag, kWaitNs)) {
                     fail();
                     break;
                 }
@@ -455,6 +473,28 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
+        if (step) {
+            // verify_attn_step: this split's share of the append (IQuestRT report, "Read only the KV tiles
+            // needed by the current positions": the new rows are written before they are read).  The
+            // live rows whose positions lie in this split's tiles go to slot pos mod slots; lanes 0..15
+            // copy 16-byte chunks of K, lanes 16..31 of V.  Every other split reads none of these rows
+            // (in a ring, a stale row of the same slot lies below every window and is zeroed or masked).
+            const int chunk = lane & 15;
+            const uint4* src = reinterpret_cast<const uint4*>(lane < 16 ? a.k_new : a.v_new) + chunk;
+            uint4* dst = reinterpret_cast<uint4*>(const_cast<uint16_t*>(lane < 16 ? a.k : a.v)) + chunk;
+            const long long tlo = P.t0 * kTile, thi = P.t1 * kTile;
+            uint4 val[kMaxRows];
+#pragma unroll
+            for (int r = 0; r < kMaxRows; ++r)
+                if (r < a.n_live && row_pos[r] >= tlo && row_pos[r] < thi) val[r] = __ldcg(src + r * (kD / 8));
+#pragma unroll
+            for (int r = 0; r < kMaxRows; ++r)
+                if (r < a.n_live && row_pos[r] >= tlo && row_pos[r] < thi)
+                    dst[(size_t)(row_pos[r] % a.slots) * (kD / 8)] = val[r];
+            ptx::fence_proxy_async_global();   // the TMA loads of these rows come after
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(ms.app_done));
+        }
         if (lane == 0) {
             constexpr uint32_t idesc_qk = ptx::idesc_bf16_f32(128, 48, 0, 0);   // A = K, B = Q: both K-major
             constexpr uint32_t idesc_pv = ptx::idesc_bf16_f32(128, 128, 1, 1);  // A = V^T, B = [P_hi | P_lo]^T: MN-major
@@ -793,12 +833,15 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
         !tc::encode_rows_map(&tmv, a.v, a.slots, 64) || !tc::encode_rows_map(&tmk2, a.k, a.slots, 128) ||
         !tc::encode_rows_map(&tmv2, a.v, a.slots, 128))
         return cudaErrorInvalidValue;
-    cudaError_t e = ensure_smem_attr((const void*)tc::attn_tc_kernel, (int)tc::kSmemBytes);
+    const bool append = a.k_new != nullptr;
+    cudaError_t e = ensure_smem_attr(append ? (const void*)tc::attn_tc_kernel<true> : (const void*)tc::attn_tc_kernel<false>,
+                                     (int)tc::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     pdl_config(&cfg, attr, dim3(a.n_splits, a.n_groups), dim3(tc::kThreads), tc::kSmemBytes, stream);
-    e = cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel, a, tmq, tmk, tmv, tmk2, tmv2);
+    e = append ? cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<true>, a, tmq, tmk, tmv, tmk2, tmv2)
+               : cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<false>, a, tmq, tmk, tmv, tmk2, tmv2);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

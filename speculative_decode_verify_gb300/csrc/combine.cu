@@ -15,12 +15,15 @@ constexpr int kQuarters = 4;                       // column quarters of a matri
 constexpr int kChunks = kD / kQuarters / 4;        // float4 chunks per quarter: 8
 constexpr int kGroups = kCombineThreads / kChunks; // split groups: 32
 constexpr int kBatch = 8;                          // splits per thread loaded together
+constexpr float kLog2e = 1.4426950408889634f;
 
 // One CTA per (matrix row m = 6 r + h, column quarter).  Thread t owns float4 chunk t % 8 of the quarter
 // and the splits s = t / 8 + 32 i: it issues all of its partial and LSE loads before using any of them.
 // Each warp merges its own splits against its own maximum (a two-level log-sum-exp merge), so the CTA
 // needs one barrier: the warp totals are then rescaled to the CTA maximum (which includes the sink) and
-// added in a fixed order: out = sum_s e^(lse_s - M) o_s / (sum_s e^(lse_s - M) + e^(sink - M)).
+// added in a fixed order: out = sum_s e^(lse_s - M) o_s / (sum_s e^(lse_s - M) + e^(sink - M)).  The
+// exponentials are the hardware exp2 of log2e-scaled differences (the library exp costs a dependent chain
+// of ~30 instructions per weight, which showed as ~1 us of the combine's time).
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* __restrict__ part_o,
                                                                   const float* __restrict__ part_lse,
                                                                   int n_splits, const float* __restrict__ sink,
@@ -67,12 +70,12 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* _
         for (int i = 0; i < kBatch; ++i) bm = fmaxf(bm, l[i]);
         for (int off = 16; off > 0; off >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, off));
         if (bm != -INFINITY) {
-            const float a = (mx == -INFINITY) ? 0.0f : expf(mx - bm);
+            const float a = (mx == -INFINITY) ? 0.0f : ptx::ex2((mx - bm) * kLog2e);
             acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
             z *= a;
 #pragma unroll
             for (int i = 0; i < kBatch; ++i) {
-                const float w = (l[i] == -INFINITY) ? 0.0f : expf(l[i] - bm);
+                const float w = (l[i] == -INFINITY) ? 0.0f : ptx::ex2((l[i] - bm) * kLog2e);
                 acc.x = fmaf(w, o[i].x, acc.x);
                 acc.y = fmaf(w, o[i].y, acc.y);
                 acc.z = fmaf(w, o[i].z, acc.z);
@@ -110,11 +113,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* _
             if (dst_lse) *dst_lse = -INFINITY;
             return;
         }
-        float sum = 0.0f, zt = (sk == -INFINITY) ? 0.0f : expf(sk - M_);
+        float sum = 0.0f, zt = (sk == -INFINITY) ? 0.0f : ptx::ex2((sk - M_) * kLog2e);
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) {
             if (wmax[w] == -INFINITY) continue;
-            const float a = expf(wmax[w] - M_);
+            const float a = ptx::ex2((wmax[w] - M_) * kLog2e);
             const float4 v = part[w][c];
             sum = fmaf(a, (e == 0) ? v.x : (e == 1) ? v.y : (e == 2) ? v.z : v.w, sum);
             zt = fmaf(a, zpart[w], zt);

@@ -28,6 +28,10 @@ struct AttnArgs {
     float scale;
     int n_rows, n_live, slots, window, n_splits;
     int n_groups;            // groups of kMaxRows rows (grid.y); 1 for chain calls
+    // verify_attn_step (chain calls only, null otherwise): the split owning a live row's position
+    // writes that row of k_new / v_new to its slot before loading the row's tile.
+    const uint16_t* k_new = nullptr;   // [n_live][128] bf16
+    const uint16_t* v_new = nullptr;
 };
 
 // Extent and split ownership derived on the device from the positions.

@@ -105,3 +105,37 @@ def expected(w: synth.Workload, n_splits: int, n_threads: int = 8):
                              w.sink.numpy(), w.scale, w.window, n_splits=n_splits, n_threads=n_threads)
     res["out_bf16"] = oracle.bf16_bits_to_f64(oracle.f64_to_bf16_bits(res["out"]))
     return res
+
+
+def run_step_fused(w: synth.Workload, n_splits: int = 0, placement: str = "all", wrap_offset: int = 0,
+                   workspace=None, variant: str = ""):
+    """The same call as run_step through verify_attn_step (append inside the attention launch, then the
+    combine).  The partials are read back from the workspace."""
+    pos_dev = (w.pos.to(torch.int64) + wrap_offset).to(torch.int32).to(DEV) if wrap_offset else w.pos.to(DEV)
+    k, v = cache_state(w, int(w.pos[0]), placement, wrap_offset)
+    q = synth.bits(w.q).to(DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    idx = w.pos[:w.n_live].to(torch.int64)
+    k_new = synth.bits(w.k_hist)[idx].contiguous().to(DEV)
+    v_new = synth.bits(w.v_hist)[idx].contiguous().to(DEV)
+    if n_splits == 0:
+        if w.window > 0:
+            n_splits = va.va_auto_splits(w.window + w.n_live - 1, w.window)
+        else:
+            n_splits = va.va_auto_splits(w.slots, 0)
+    if workspace is None:
+        workspace = torch.full((va.va_workspace_bytes(n_splits) // 4,), float("nan"), dtype=torch.float32,
+                               device=DEV)
+    out = torch.full((w.n_rows, 6, 128), 0x7FC0, dtype=torch.int16, device=DEV)
+    out_lse = torch.full((w.n_rows, 6), float("nan"), dtype=torch.float32, device=DEV)
+    used = va.verify_attn_step(q, k_new, v_new, w.n_live, k, v, pos_dev, w.scale, w.sink.to(DEV), workspace, out,
+                               out_lse, window=w.window, n_splits=n_splits, dev_status=status, variant=variant)
+    assert used == n_splits
+    torch.cuda.synchronize()
+    n_o = n_splits * 8 * 6 * 128       # part_lse starts after room for 8 rows per split
+    part_o = workspace[:n_splits * w.n_rows * 6 * 128].view(n_splits, w.n_rows, 6, 128)
+    part_lse = workspace[n_o:n_o + n_splits * w.n_rows * 6].view(n_splits, w.n_rows, 6)
+    return dict(out=oracle.bf16_bits_to_f64(out.cpu().numpy()), out_bits=out.cpu().numpy().view(np.uint16),
+                out_lse=out_lse.cpu().numpy().astype(np.float64), part_o=part_o.cpu().numpy().astype(np.float64),
+                part_lse=part_lse.cpu().numpy().astype(np.float64), n_splits=n_splits,
+                status=int(status.item()), k=k, v=v, workspace=workspace)

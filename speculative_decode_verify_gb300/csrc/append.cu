@@ -6,7 +6,9 @@
 
 namespace va {
 
-// One warp per live row: lanes 0..15 copy K (16 B each), lanes 16..31 copy V.
+// One warp per live row: lanes 0..15 copy K (16 B each), lanes 16..31 copy V.  The rows land as if written
+// in row order: a row whose slot a later row also writes is skipped (rows <= 16, so lane l holds row l's
+// position).
 __global__ void __launch_bounds__(32) kv_append_kernel(const uint4* __restrict__ k_new,
                                                        const uint4* __restrict__ v_new,
                                                        uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
@@ -18,14 +20,17 @@ __global__ void __launch_bounds__(32) kv_append_kernel(const uint4* __restrict__
     ptx::griddep_wait();   // every global access comes after this
     constexpr int kChunks = kD * 2 / 16;   // 16 chunks of 16 B per row
     const int c = lane & (kChunks - 1);
-    // the row and its position are loaded together (one memory round trip)
+    // the row and the positions are loaded together (one memory round trip)
+    const int n = gridDim.x;
     const uint4 val = lane < kChunks ? __ldcg(k_new + (long long)r * kChunks + c) : __ldcg(v_new + (long long)r * kChunks + c);
-    const int p = __ldcg(pos + r);
+    const int pl = lane < n ? __ldcg(pos + lane) : -1;
+    const int p = __shfl_sync(0xffffffffu, pl, r);
     if (p < 0) {
         if (lane == 0 && dev_status) atomicOr(dev_status, VA_DEV_NEGATIVE_POS);
         return;
     }
     const long long slot = (long long)p % slots;
+    if (__any_sync(0xffffffffu, lane > r && pl >= 0 && (long long)pl % slots == slot)) return;
     if (lane < kChunks)
         k_cache[slot * kChunks + c] = val;
     else

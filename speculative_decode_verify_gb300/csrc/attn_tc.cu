@@ -346,8 +346,8 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
         if (kPrefetch > 0 && j >= kNV && j + kPrefetch < ntiles) prefetch_tile(&tmv, &tmv2, j + kPrefetch);
     };
     // verify_attn_step: a tile holding a live row's position is loaded only after the MMA warp, which
-    // appends this split's live rows, has written them (app_done).  Positions are increasing, so the live
-    // rows are the positions [pos[0], hi).
+    // appends this split's live rows first, has written them (app_done).  Positions never decrease, so the
+    // live rows are the positions [pos[0], hi).
     constexpr bool step = kAppend;
     auto tile_has_new = [&](int j) {
         if (!step) return false;
@@ -475,23 +475,33 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
         // ------------------------------------------------------------ MMA issuer
         if (step) {
             // verify_attn_step: this split's share of the append (IQuestRT report, "Read only the KV tiles
-            // needed by the current positions": the new rows are written before they are read).  The
-            // live rows whose positions lie in this split's tiles go to slot pos mod slots; lanes 0..15
-            // copy 16-byte chunks of K, lanes 16..31 of V.  Every other split reads none of these rows
-            // (in a ring, a stale row of the same slot lies below every window and is zeroed or masked).
-            const int chunk = lane & 15;
-            const uint4* src = reinterpret_cast<const uint4*>(lane < 16 ? a.k_new : a.v_new) + chunk;
-            uint4* dst = reinterpret_cast<uint4*>(const_cast<uint16_t*>(lane < 16 ? a.k : a.v)) + chunk;
+            // needed by the current positions": the new rows are written before they are read).  The live
+            // rows whose positions lie in this split's tiles go to slot pos mod slots; a row whose slot a
+            // later row also writes is skipped, so the rows land as if written in row order.  Every other
+            // split reads none of these rows (in a ring, a stale row of the same slot lies below every
+            // window and is zeroed or masked).  Only a split that owns live rows waits for its stores
+            // (the proxy fence) before its first product.
+            const uint4* src = reinterpret_cast<const uint4*>(lane < 16 ? a.k_new : a.v_new) + (lane & 15);
+            uint4* dst = reinterpret_cast<uint4*>(const_cast<uint16_t*>(lane < 16 ? a.k : a.v)) + (lane & 15);
             const long long tlo = P.t0 * kTile, thi = P.t1 * kTile;
+            bool mine[kMaxRows];
             uint4 val[kMaxRows];
+            bool any = false;
 #pragma unroll
-            for (int r = 0; r < kMaxRows; ++r)
-                if (r < a.n_live && row_pos[r] >= tlo && row_pos[r] < thi) val[r] = __ldcg(src + r * (kD / 8));
+            for (int r = 0; r < kMaxRows; ++r) {
+                // the plan accepted the positions: they never decrease and span less than the slots, so
+                // rows share a slot only when they share a position, and then they are adjacent
+                mine[r] = r < a.n_live && row_pos[r] >= tlo && row_pos[r] < thi &&
+                          !(r + 1 < kMaxRows && r + 1 < a.n_live && row_pos[r + 1] == row_pos[r]);
+                if (mine[r]) val[r] = __ldcg(src + r * (kD / 8));
+                any |= mine[r];
+            }
+            if (any) {   // (most splits own no live row and skip the stores and the fence)
 #pragma unroll
-            for (int r = 0; r < kMaxRows; ++r)
-                if (r < a.n_live && row_pos[r] >= tlo && row_pos[r] < thi)
-                    dst[(size_t)(row_pos[r] % a.slots) * (kD / 8)] = val[r];
-            ptx::fence_proxy_async_global();   // the TMA loads of these rows come after
+                for (int r = 0; r < kMaxRows; ++r)
+                    if (mine[r]) dst[(size_t)(row_pos[r] % a.slots) * (kD / 8)] = val[r];
+                ptx::fence_proxy_async_global();   // the TMA loads of these rows come after
+            }
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(ms.app_done));
         }

@@ -128,6 +128,27 @@ def test_no_live_rows_gives_zero():
     assert torch.all(out == 0) and torch.all(torch.isneginf(part_lse)) and torch.all(part_o == 0)
 
 
+@pytest.mark.parametrize("pos", [[5, 7, 7, 9, 9, 9, 12, 13], [3, 259, 4, 515, 6, 6, 100, 3],
+                                 list(range(16)), [40] * 16])
+def test_append_rows_sharing_a_slot_land_in_row_order(pos):
+    # repeated positions, and positions a multiple of the slot count apart: the last row wins
+    slots = 256
+    g = synth.generator(24)
+    n = len(pos)
+    k0 = torch.randint(-30000, 30000, (slots, 128), generator=g, dtype=torch.int16)
+    v0 = torch.randint(-30000, 30000, (slots, 128), generator=g, dtype=torch.int16)
+    kn = torch.randint(-30000, 30000, (n, 128), generator=g, dtype=torch.int16)
+    vn = torch.randint(-30000, 30000, (n, 128), generator=g, dtype=torch.int16)
+    p = torch.tensor(pos, dtype=torch.int32)
+    for _ in range(3):
+        k, v = k0.clone().to(DEV), v0.clone().to(DEV)
+        va.kv_ring_append(kn.to(DEV), vn.to(DEV), n, k, v, p.to(DEV))
+        ek, ev = oracle.ring_append(k0.numpy(), v0.numpy(), kn.numpy(), vn.numpy(), p.numpy(), n)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(k.cpu().numpy(), ek)
+        np.testing.assert_array_equal(v.cpu().numpy(), ev)
+
+
 def test_append_bytes_bit_exact_with_wrap():
     slots = 256
     g = synth.generator(23)

@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import parity
 import speculative_decode_verify_gb300 as va
 from gpu_cases import DEV, expected, run_step, run_step_fused
@@ -158,3 +159,29 @@ def test_step_argument_errors():
     with pytest.raises(va.VerifyAttnError) as e:
         va.verify_attn_step(q, kn, kn, 8, ring, ring, pos, w.scale, sink, ws, out, window=4096, n_splits=4)
     assert e.value.status == va.VA_UNSUPPORTED
+
+
+def test_step_append_with_repeated_positions_matches_row_order():
+    # rows sharing a position: the last of them is the one left in the cache, as kv_ring_append leaves it
+    w = synth.make("dup", 80, ctx=700, n_live=5, slots=768,
+                   pos=torch.tensor([600, 601, 601, 602, 602, 603, 604, 605], dtype=torch.int32))
+    kn = torch.randint(-2000, 2000, (5, 128), dtype=torch.int16, generator=synth.generator(81))
+    vn = torch.randint(-2000, 2000, (5, 128), dtype=torch.int16, generator=synth.generator(82))
+    k0 = torch.zeros(768, 128, dtype=torch.int16)
+    k0[:w.ctx] = synth.bits(w.k_hist)
+    v0 = torch.zeros(768, 128, dtype=torch.int16)
+    v0[:w.ctx] = synth.bits(w.v_hist)
+    pos = w.pos.to(DEV)
+    ka, va_ = k0.to(DEV), v0.to(DEV)
+    va.kv_ring_append(kn.to(DEV), vn.to(DEV), 5, ka, va_, pos)
+    kb, vb = k0.to(DEV), v0.to(DEV)
+    ws = torch.empty(va.va_workspace_bytes(3) // 4, dtype=torch.float32, device=DEV)
+    out = torch.empty(8, 6, 128, dtype=torch.int16, device=DEV)
+    va.verify_attn_step(synth.bits(w.q).to(DEV), kn.to(DEV), vn.to(DEV), 5, kb, vb, pos, w.scale, w.sink.to(DEV), ws,
+                        out, n_splits=3)
+    torch.cuda.synchronize()
+    ek, ev = oracle.ring_append(k0.numpy(), v0.numpy(), kn.numpy(), vn.numpy(), w.pos.numpy(), 5)
+    np.testing.assert_array_equal(kb.cpu().numpy(), ek)
+    np.testing.assert_array_equal(vb.cpu().numpy(), ev)
+    assert torch.equal(ka, kb) and torch.equal(va_, vb)
+    assert torch.equal(kb[601].cpu(), kn[2]) and torch.equal(kb[602].cpu(), kn[4])

@@ -495,14 +495,38 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
             const long long kbase = t * kTile;
             const long long kp = kbase + L;
             const int sb = j & 1, ks = j % kNK, vs = j % kNV;
-            if (!ptx::mbar_wait(bar(ms.s_full[sb]), (j >> 1) & 1, abort_flag, kWaitNs)) ok = false;
-            ptx::tc_fence_after();
-            float x[kCols];
-            ptx::tmem_ld24_wait(tl + (sb ? kColS1 : kColS0) + n0, x);
-            ptx::tc_fence_before();
+            // V of this tile first, while QK(j) runs: its scales, then its codes widened to fp16 (key L, d half
+            // ch) into the fp16 buffer of this tile's parity once the PV two tiles back has read it; then the
+            // code stage is free
+            if (!ptx::mbar_wait(bar(ms.v_full[vs]), (j / kNV) & 1, abort_flag, kWaitNs)) ok = false;
+            const float sv = ms.vscale[vs][L];
+            const bool own = L < nkeys && kp >= own_lo && kp < own_hi;
+            uint4 raw[4];
+            {
+                const uint32_t roff = kOffV + (uint32_t)vs * kStage + (uint32_t)(L >> 3) * 1024u + (uint32_t)(L & 7) * 128u;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    raw[c] = *reinterpret_cast<const uint4*>(base + roff + (((uint32_t)(4 * ch + c) ^ (uint32_t)(L & 7)) << 4));
+            }
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(ms.s_free[sb]));
-            const float sk = ms.kscale[ks][L];
+            if (lane == 0) ptx::mbar_arrive(bar(ms.v_empty[vs]));
+            if (j >= 2 && !ptx::mbar_wait(bar(ms.pv_done[j & 1]), ((j - 2) >> 1) & 1, abort_flag, kWaitNs)) ok = false;
+            {
+                const uint32_t woff = kOffV16 + (uint32_t)(j & 1) * kV16 + (uint32_t)ch * kV16Half +
+                                      (uint32_t)(L >> 3) * 1024u + (uint32_t)(L & 7) * 128u;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint4 h0, h1;   // 16 codes -> two 16-byte chunks of 8 fp16 values
+                    int8x4_to_half(raw[c].x, h0.x, h0.y);
+                    int8x4_to_half(raw[c].y, h0.z, h0.w);
+                    int8x4_to_half(raw[c].z, h1.x, h1.y);
+                    int8x4_to_half(raw[c].w, h1.z, h1.w);
+                    if (!own) h0 = h1 = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(base + woff + (((uint32_t)(2 * c) ^ (uint32_t)(L & 7)) << 4)) = h0;
+                    *reinterpret_cast<uint4*>(base + woff + (((uint32_t)(2 * c + 1) ^ (uint32_t)(L & 7)) << 4)) = h1;
+                }
+            }
+            // which of the rows of this column half see key L (no score needed)
             const bool interior = kbase >= all_lo && kbase + nkeys <= all_hi;
             bool vis[kCols];
             {
@@ -515,6 +539,14 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
 #pragma unroll
                 for (int i = 0; i < kCols; ++i) vis[i] = rv[i / kH];
             }
+            if (!ptx::mbar_wait(bar(ms.s_full[sb]), (j >> 1) & 1, abort_flag, kWaitNs)) ok = false;
+            ptx::tc_fence_after();
+            float x[kCols];
+            ptx::tmem_ld24_wait(tl + (sb ? kColS1 : kColS0) + n0, x);
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(ms.s_free[sb]));
+            const float sk = ms.kscale[ks][L];
 #pragma unroll
             for (int i = 0; i < kCols; ++i) x[i] *= sk;   // score = x * cq[i] in log2 units
             if (j == 0) {
@@ -582,36 +614,6 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
 #pragma unroll
             for (int i = 0; i < kCols; ++i) l[i] += p[i];
 
-            // V of this tile: its scales, then its codes widened to fp16 (key L, d half ch) into the fp16
-            // buffer of this tile's parity once the PV two tiles back has read it; then the code stage is free
-            if (!ptx::mbar_wait(bar(ms.v_full[vs]), (j / kNV) & 1, abort_flag, kWaitNs)) ok = false;
-            const float sv = ms.vscale[vs][L];
-            const bool own = L < nkeys && kp >= own_lo && kp < own_hi;
-            uint4 raw[4];
-            {
-                const uint32_t roff = kOffV + (uint32_t)vs * kStage + (uint32_t)(L >> 3) * 1024u + (uint32_t)(L & 7) * 128u;
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    raw[c] = *reinterpret_cast<const uint4*>(base + roff + (((uint32_t)(4 * ch + c) ^ (uint32_t)(L & 7)) << 4));
-            }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(ms.v_empty[vs]));
-            if (j >= 2 && !ptx::mbar_wait(bar(ms.pv_done[j & 1]), ((j - 2) >> 1) & 1, abort_flag, kWaitNs)) ok = false;
-            {
-                const uint32_t woff = kOffV16 + (uint32_t)(j & 1) * kV16 + (uint32_t)ch * kV16Half +
-                                      (uint32_t)(L >> 3) * 1024u + (uint32_t)(L & 7) * 128u;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint4 h0, h1;   // 16 codes -> two 16-byte chunks of 8 fp16 values
-                    int8x4_to_half(raw[c].x, h0.x, h0.y);
-                    int8x4_to_half(raw[c].y, h0.z, h0.w);
-                    int8x4_to_half(raw[c].z, h1.x, h1.y);
-                    int8x4_to_half(raw[c].w, h1.z, h1.w);
-                    if (!own) h0 = h1 = make_uint4(0u, 0u, 0u, 0u);
-                    *reinterpret_cast<uint4*>(base + woff + (((uint32_t)(2 * c) ^ (uint32_t)(L & 7)) << 4)) = h0;
-                    *reinterpret_cast<uint4*>(base + woff + (((uint32_t)(2 * c + 1) ^ (uint32_t)(L & 7)) << 4)) = h1;
-                }
-            }
             // P' = p * v_scale as fp16, over this tile's K codes (QK(j) has read them)
             uint32_t pw[kCols / 2];
 #pragma unroll

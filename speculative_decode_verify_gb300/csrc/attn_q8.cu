@@ -61,8 +61,11 @@ constexpr int kSoftWarp0 = 3;
 constexpr int kThreads = 32 * (kSoftWarp0 + kSoftWarps);
 constexpr int kSoftThreads = 32 * kSoftWarps;
 constexpr int kCols = kMaxM / 2;
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS0 = 0, kColS1 = 64, kColO = 128;
+// S^T of a tile is three 48-column blocks, one per E4M3 term of q (QK runs as one N = 144 MMA per k-step,
+// so that each K slice is read once), double-buffered; then O^T (48 columns).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS0 = 0, kColS1 = 160, kColO = 320;
+constexpr uint32_t kTermCols = 48;
 constexpr float kThresh = 256.0f;
 constexpr float kRefInit = -1.0e30f;
 constexpr uint64_t kWaitNs = 2000000000ull;
@@ -341,7 +344,7 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             // QK: A = K codes, B = q terms, both E4M3 K-major; PV: A = V^T fp16, B = P'^T fp16, MN-major
-            constexpr uint32_t idesc_qk = (1u << 4) | (0u << 7) | (0u << 10) | ((48u >> 3) << 17) | ((128u >> 4) << 24);
+            constexpr uint32_t idesc_qk = (1u << 4) | (0u << 7) | (0u << 10) | ((144u >> 3) << 17) | ((128u >> 4) << 24);
             constexpr uint32_t idesc_pv =
                 (1u << 4) | (0u << 7) | (0u << 10) | (1u << 15) | (1u << 16) | ((48u >> 3) << 17) | ((128u >> 4) << 24);
             // rotation: (H q)^T [128 x 48] = H . q^T into the first S buffer (A = H, B = q: bf16, K-major)
@@ -369,17 +372,16 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
                     const int ks = qk % kNK, sb = qk & 1;
                     ptx::tc_fence_after();
                     const uint32_t d = tmem + (sb ? kColS1 : kColS0);
+                    // B = the three q terms as 144 consecutive K-major rows (each term 48 rows, 6 KB)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-                        for (int t = 0; t < 3; ++t)
-                            asm volatile(
-                                "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-                                " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-                                "l"(ptx::smem_desc(base_s + kOffK + ks * kStage + kk * 32, 0, 1024)),
-                                "l"(ptx::smem_desc(base_s + kOffQ + t * kQTerm + kk * 32, 0, 1024)), "r"(idesc_qk),
-                                "r"((kk > 0 || t > 0) ? 1u : 0u)
-                                : "memory");
+                        asm volatile(
+                            "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                            " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+                            "l"(ptx::smem_desc(base_s + kOffK + ks * kStage + kk * 32, 0, 1024)),
+                            "l"(ptx::smem_desc(base_s + kOffQ + kk * 32, 0, 1024)), "r"(idesc_qk),
+                            "r"(kk > 0 ? 1u : 0u)
+                            : "memory");
                     ptx::mma_commit(bar(ms.s_full[sb]));
                     ++qk;
                     progressed = true;
@@ -542,7 +544,17 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
             if (!ptx::mbar_wait(bar(ms.s_full[sb]), (j >> 1) & 1, abort_flag, kWaitNs)) ok = false;
             ptx::tc_fence_after();
             float x[kCols];
-            ptx::tmem_ld24_wait(tl + (sb ? kColS1 : kColS0) + n0, x);
+            {   // the three terms' scores, added
+                const uint32_t sc = tl + (sb ? kColS1 : kColS0) + n0;
+                float y[kCols];
+                ptx::tmem_ld24_wait(sc, x);
+#pragma unroll
+                for (int t = 1; t < 3; ++t) {
+                    ptx::tmem_ld24_wait(sc + t * kTermCols, y);
+#pragma unroll
+                    for (int i = 0; i < kCols; ++i) x[i] += y[i];
+                }
+            }
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(ms.s_free[sb]));

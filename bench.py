@@ -222,6 +222,13 @@ def cpu_baseline(w_full):
                       f"(all 48 row-head pairs, FP64), {cores} threads, {per_call * 1e3:.1f} ms/call"}
 
 
+def workload_config():
+    """The workload both arms report (the GPU arm adds how it ran it)."""
+    return {"workload": "full-attention verify, 196,608 positions (100.7 MB bf16 K/V), 1 KV head / 6 q heads, d 128, "
+                        "8 rows with n_live 4,5,6,7,8 (one call each per step)",
+            "calls_per_step": len(N_LIVES), "capacity": CAPACITY}
+
+
 def reference_arm(args, dist: Dist):
     if dist.rank != 0:
         return
@@ -245,8 +252,8 @@ def reference_arm(args, dist: Dist):
                       "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
                       "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                       "data": "synthetic",
-                      "config": {"workload": "full attention verify call, 1 KV head / 6 q heads, d 128, 8 rows "
-                                             "(oracle sample: 4,096-position prefix)"},
+                      "config": dict(workload_config(), timing="wall clock on the host cores, a bounded sample "
+                                                                               "per step (cpu_baseline.sample)"),
                       "cpu_baseline": {"value": value, "unit": "GB/s", "kind": "oracle", "cores": cores,
                                        "sample": sample},
                       "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
@@ -790,13 +797,11 @@ def ours(args, dist: Dist):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": dist.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": t_max / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": "full-attention verify, 196,608 positions (100.7 MB bf16 K/V), 1 KV head / 6 q "
-                               "heads, d 128, 8 rows with n_live 4,5,6,7,8 (one call each per step)",
-                   "calls_per_step": len(calls), "n_splits": S, "capacity": CAPACITY,
+        "config": dict(workload_config(), **{"n_splits": S,
                    "l2": "5 distinct 100.7 MB caches rotate: each call reads K/V untouched for ~400 MB of "
                          "traffic, larger than L2 (no flush)",
                    "timing": "CUDA graph of the step replayed K times, CUDA events on its stream",
-                   "parallelism": f"replicas x{dist.world} (one KV head per GPU, no collective)"},
+                   "parallelism": f"replicas x{dist.world} (one KV head per GPU, no collective)"}),
         "us_per_call": t_max / args.steps / len(calls) * 1e6,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": measured_traffic(), "kernel": "verify_attn_full split kernel",

@@ -367,13 +367,14 @@ def ours(args, dist: Dist):
         for c in calls:
             launch_call(c)
 
-    def sweep_point(ctx, window, reps=200):
-        """us per call and algorithmic GB/s of one verify call (append + attention + combine, graph
-        replay) at this context; two caches alternate so K/V are read cold when they exceed L2."""
-        n = 8
+    def sweep_points(ctx, window, reps=200):
+        """us per call and algorithmic GB/s of one verify call (verify_attn_step with the library's split
+        choice, graph replay) at this context for n_live 4..8; two caches alternate so K/V are read cold
+        when they exceed L2.  The caches hold the whole history, so every n_live uses the same ones (the
+        append rewrites the live rows with their own values)."""
         ws = []
         for rep in range(2):
-            w = synth.make(f"sweep{ctx}", 900 + rep, ctx=ctx, n_live=n, window=window,
+            w = synth.make(f"sweep{ctx}", 900 + rep, ctx=ctx, n_live=8, window=window,
                            slots=(synth.RING_SLOTS if window else ctx + 64))
             slots = w.slots
             k = torch.full((slots, 128), synth.BF16_NAN, dtype=torch.int16)
@@ -383,43 +384,50 @@ def ours(args, dist: Dist):
             pp = torch.arange(first, ctx)
             k[pp % slots] = kb[first:ctx]
             v[pp % slots] = vb[first:ctx]
-            idx = w.pos[:n].to(torch.int64)
-            ws.append(dict(w=w, k=k.to(dev), v=v.to(dev), q=synth.bits(w.q).to(dev), pos=w.pos.to(dev),
-                           sink=w.sink.to(dev), kn=kb[idx].contiguous().to(dev), vn=vb[idx].contiguous().to(dev),
-                           out=torch.empty(8, 6, 128, dtype=torch.int16, device=dev)))
-        Ss = va.va_auto_splits(window + n - 1 if window else ctx, window)
-        wsp = torch.empty(va.va_workspace_bytes(Ss) // 4, dtype=torch.float32, device=dev)
+            ws.append(dict(w=w, k=k.to(dev), v=v.to(dev), kb=kb, vb=vb, q=synth.bits(w.q).to(dev),
+                           sink=w.sink.to(dev), out=torch.empty(8, 6, 128, dtype=torch.int16, device=dev)))
+        hbm = (measured_peaks() or {}).get("hbm_gbs", 6800.0)
+        points = []
+        for n in N_LIVES:
+            for c in ws:
+                pos = synth.tail_positions(ctx, n)
+                idx = pos[:n].to(torch.int64)
+                c["pos"] = pos.to(dev)
+                c["kn"], c["vn"] = c["kb"][idx].contiguous().to(dev), c["vb"][idx].contiguous().to(dev)
+            Ss = va.va_auto_splits(window + n - 1 if window else ctx, window)
+            wsp = torch.empty(va.va_workspace_bytes(Ss) // 4, dtype=torch.float32, device=dev)
 
-        def one(c):
-            w = c["w"]
-            st = L.verify_attn_step(P(c["q"].data_ptr()), P(c["kn"].data_ptr()), P(c["vn"].data_ptr()), 8, n,
-                                    P(c["k"].data_ptr()), P(c["v"].data_ptr()), w.slots, window,
-                                    P(c["pos"].data_ptr()), P(c["sink"].data_ptr()), ctypes.c_float(w.scale), Ss,
-                                    P(wsp.data_ptr()), P(c["out"].data_ptr()), None, None, None, sp)
-            if st:
-                raise RuntimeError(f"sweep call failed with status {st}")
+            def one(c):
+                w = c["w"]
+                st = L.verify_attn_step(P(c["q"].data_ptr()), P(c["kn"].data_ptr()), P(c["vn"].data_ptr()), 8, n,
+                                        P(c["k"].data_ptr()), P(c["v"].data_ptr()), w.slots, window,
+                                        P(c["pos"].data_ptr()), P(c["sink"].data_ptr()), ctypes.c_float(w.scale),
+                                        Ss, P(wsp.data_ptr()), P(c["out"].data_ptr()), None, None, None, sp)
+                if st:
+                    raise RuntimeError(f"sweep call failed with status {st}")
 
-        with torch.cuda.stream(stream):
-            for _ in range(3):
-                for c in ws:
-                    one(c)
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for c in ws:
-                    one(c)
-            g.replay()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(reps):
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    for c in ws:
+                        one(c)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for c in ws:
+                        one(c)
                 g.replay()
-            e1.record(stream)
-            e1.synchronize()
-        us = e0.elapsed_time(e1) * 1e3 / (reps * 2)
-        hi = ctx
-        lo = max(0, ctx - n - window + 1) if window else 0
-        nbytes = 512 * (hi - lo) + Q_BYTES + OUT_BYTES + 2 * 512 * n + 24
-        return {"ctx": ctx, "kind": "swa" if window else "full", "n_live": n, "splits": Ss, "us_per_call": us,
-                "gbs": nbytes / us / 1e3}
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(reps):
+                    g.replay()
+                e1.record(stream)
+                e1.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (reps * 2)
+            hi = ctx
+            lo = max(0, ctx - n - window + 1) if window else 0
+            nbytes = 512 * (hi - lo) + Q_BYTES + OUT_BYTES + 2 * 512 * n + 24
+            points.append({"ctx": ctx, "kind": "swa" if window else "full", "n_live": n, "splits": Ss,
+                           "us_per_call": us, "gbs": nbytes / us / 1e3, "frac_of_hbm_peak": nbytes / us / 1e3 / hbm})
+        return points
 
     def tree_measure(reps=300):
         """A 16-node best-first draft tree at the 192K extent (nodes at 196,592..196,607): per call
@@ -783,7 +791,7 @@ def ours(args, dist: Dist):
     if not args.no_sweep:
         for ctx_s in synth.SWEEP_CONTEXTS:
             for window in (0, synth.WINDOW):
-                sweep.append(sweep_point(ctx_s, window))
+                sweep.extend(sweep_points(ctx_s, window))
     step_bytes = sum(call_bytes(c["hi"], c["n"]) for c in calls)
     value, t_max = aggregate(step_bytes * args.steps / 1e9, t_graph, dist)
     e2e_value, _ = aggregate(step_bytes * ke / 1e9, t_e2e, dist)

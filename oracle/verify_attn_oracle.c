@@ -123,7 +123,7 @@ static int visible(const job_t *J, int r, int64_t j)
 static void one_pair(job_t *J, int r, int h, double *scores)
 {
     int64_t first = row_first(J, r);
-    if (J->tree && first > J->tree[0]) first = J->tree[0];   /* node slots are judged by visible() alone */
+    if (J->tree && first > J->tree[0]) first = J->tree[0];   /* node slots are decided by visible() alone */
     const int64_t p = J->pos[r];   /* tree: base + n_nodes - 1, the last slot any node may see */
     const int64_t n = p - first + 1;
     double qd[OR_D];

@@ -574,11 +574,78 @@ def ours(args, dist: Dist):
         hi = statistics.fmean(int(c["pos"][c["n"] - 1]) + 1 for c in qs)
         attn_b = 264 * hi + Q_BYTES
         peak = (measured_peaks() or {}).get("hbm_gbs", 6800.0)
+        tree = q8_tree_measure(qs, reps)
+        tree["attn_frac_of_hbm_peak"] = tree["attn_gbs"] / peak
         return {"workload": "quantised cache (E4M3 keys after a Hadamard rotation, INT8 values, fp32 row scales: "
                             "264 B per position), 196,608 positions (51.9 MB), 3 rotating caches",
                 "n_splits": S, "attn_us_per_launch": us_attn, "attn_gbs": attn_b / us_attn / 1e3,
                 "attn_frac_of_hbm_peak": attn_b / us_attn / 1e3 / peak, "us_per_call": us_call,
-                "bytes_per_position": 264}
+                "bytes_per_position": 264, "tree": tree}
+
+    def q8_tree_measure(qs, reps):
+        """A 16-node best-first draft tree over the same quantised caches, nodes at 196,592..196,607: the
+        tree attention launch alone back to back, and the whole call (encoding append of the 16 nodes +
+        verify_attn_q8_tree + combine) graph-replayed."""
+        groups = 2
+        St = va.va_auto_splits_for(CAPACITY, 0, torch.cuda.get_device_properties(dev).multi_processor_count // groups)
+        po = torch.empty(St, 16, 6, 128, dtype=torch.float32, device=dev)
+        pl = torch.empty(St, 16, 6, dtype=torch.float32, device=dev)
+        ts = []
+        for i, c in enumerate(qs):
+            tw = synth.make_tree(f"bench_q8tree{i}", 520 + i, base=0, n_nodes=16)   # q, masks, nodes' K/V
+            tree = tw.tree.clone()
+            tree[0] = CTX - 16
+            ts.append(dict(c=c, tw=tw, tree=tree.to(dev), q=synth.bits(tw.q).to(dev),
+                           kn=synth.bits(tw.k_hist).contiguous().to(dev), vn=synth.bits(tw.v_hist).contiguous().to(dev),
+                           pos=torch.arange(CTX - 16, CTX, dtype=torch.int32, device=dev), sink=tw.sink.to(dev),
+                           out=torch.empty(16, 6, 128, dtype=torch.int16, device=dev)))
+
+        def attn(t):
+            c = t["c"]
+            return L.verify_attn_q8_tree(P(t["q"].data_ptr()), 16, 16, P(c["kc"].data_ptr()), P(c["vc"].data_ptr()),
+                                         P(c["ks"].data_ptr()), P(c["vs"].data_ptr()), CAPACITY, 0,
+                                         P(t["tree"].data_ptr()), ctypes.c_float(t["tw"].scale), St, P(po.data_ptr()),
+                                         P(pl.data_ptr()), None, None, sp)
+
+        def one(t):
+            c = t["c"]
+            st = L.kv_ring_append_q8(P(t["kn"].data_ptr()), P(t["vn"].data_ptr()), 16, P(c["kc"].data_ptr()),
+                                     P(c["vc"].data_ptr()), P(c["ks"].data_ptr()), P(c["vs"].data_ptr()), CAPACITY,
+                                     P(t["pos"].data_ptr()), None, sp)
+            st |= attn(t)
+            st |= L.attn_split_combine(P(po.data_ptr()), P(pl.data_ptr()), St, P(t["sink"].data_ptr()), 16, 16,
+                                       P(t["out"].data_ptr()), None, sp)
+            if st:
+                raise RuntimeError(f"quantised tree call failed with status {st}")
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                for t in ts:
+                    one(t)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                for t in ts:
+                    if attn(t):
+                        raise RuntimeError("verify_attn_q8_tree failed")
+            e1.record(stream)
+            e1.synchronize()
+            us_attn = e0.elapsed_time(e1) * 1e3 / (reps * len(ts))
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for t in ts:
+                    one(t)
+            g.replay()
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            us_call = e0.elapsed_time(e1) * 1e3 / (reps * len(ts))
+        attn_b = 264 * CTX + 16 * 6 * 128 * 2 + 17 * 4
+        return {"workload": "16-node best-first draft tree, nodes at 196,592..196,607 of the quantised 196,608-"
+                            "position cache", "n_splits": St, "groups": groups, "attn_us_per_launch": us_attn,
+                "attn_gbs": attn_b / us_attn / 1e3, "us_per_call": us_call}
 
     def post_verify_measure(reps=400):
         """The calls after verification, each graph-replayed: top-k 20 / top-p 0.95 sampling of 8 rows of

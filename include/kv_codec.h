@@ -53,6 +53,26 @@ VA_API va_status verify_attn_q8(const va_bf16 *q, int n_rows, int n_live, const 
                                 int window, const int32_t *pos, float scale, int n_splits, float *part_o,
                                 float *part_lse, int *splits_used, int32_t *dev_status, va_stream stream);
 
+/*
+ * verify_attn_q8_tree - verify attention of a draft TREE over the quantised cache.
+ * Source: "Qwen3.8-27B on one RTX 4090": the 16-node verify trees of "More tokens per round: verify
+ * trees" read the cache of "A cheaper cache and state".  The kernel is verify_attn_q8's with each node's
+ * ancestor mask in place of the causal tail (the masks, extent and split plan of verify_attn_tree); up
+ * to 16 nodes run as two groups of 8 rows.
+ *   q, n_rows, n_nodes, window, tree, scale  as verify_attn_tree (n_rows 1..16; window 0 or >= n_nodes)
+ *   k_codes, v_codes, k_scale, v_scale, slots  the quantised cache as for verify_attn_q8 (slots a
+ *                 multiple of 64, else VA_UNSUPPORTED; window > 0: slots >= window + n_nodes - 1, else
+ *                 VA_RING_TOO_SMALL).  Node i's codes sit at position base + i: append them first
+ *                 (kv_ring_append_q8 with pos[i] = base + i, same stream).
+ *   n_splits      1..VA_MAX_SPLITS, or 0 = auto (the ceil(n_rows / 8) node groups share the SMs)
+ *   part_o, part_lse, splits_used, dev_status  as verify_attn_tree; merge with attn_split_combine
+ * Returns VA_OK, VA_INVALID_ARG, VA_UNSUPPORTED, VA_RING_TOO_SMALL or VA_CUDA_ERROR.
+ */
+VA_API va_status verify_attn_q8_tree(const va_bf16 *q, int n_rows, int n_nodes, const uint8_t *k_codes,
+                                     const int8_t *v_codes, const float *k_scale, const float *v_scale, int slots,
+                                     int window, const int32_t *tree, float scale, int n_splits, float *part_o,
+                                     float *part_lse, int *splits_used, int32_t *dev_status, va_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

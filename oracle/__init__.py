@@ -90,6 +90,10 @@ def _load():
             lib.oracle_verify_attn_f64kv.argtypes = [p, p, p, ctypes.c_int64, p, ctypes.c_int, ctypes.c_int, p,
                                                      ctypes.c_double, ctypes.c_int64, ctypes.c_int, p, p,
                                                      p, p, p, p, ctypes.c_int]
+            lib.oracle_verify_attn_tree_f64kv.restype = ctypes.c_int
+            lib.oracle_verify_attn_tree_f64kv.argtypes = [p, p, p, ctypes.c_int64, p, ctypes.c_int, ctypes.c_int,
+                                                          p, ctypes.c_double, ctypes.c_int64, ctypes.c_int, p, p,
+                                                          p, p, p, p, ctypes.c_int]
             lib.oracle_combine.restype = ctypes.c_int
             lib.oracle_combine.argtypes = [p, p, ctypes.c_int, p, ctypes.c_int, ctypes.c_int, p, p]
             _lib = lib

@@ -24,10 +24,10 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import _load, _ptr, split_position_ranges, read_extent, Q_HEADS, HEAD_DIM
+from . import _load, _ptr, split_position_ranges, read_extent, tree_extent, Q_HEADS, HEAD_DIM
 
 __all__ = ["E4M3_MAX", "fwht_f32", "e4m3_round", "e4m3_decode", "e4m3_encode_bits", "encode_k", "encode_v",
-           "decode_k", "decode_v", "verify_attn_decoded"]
+           "decode_k", "decode_v", "verify_attn_decoded", "verify_attn_tree_decoded"]
 
 E4M3_MAX = 448.0
 
@@ -161,4 +161,38 @@ def verify_attn_decoded(q_bits, k_dec, v_dec, pos, n_live: int, sink, scale: flo
                                           _ptr(lse), _ptr(part_o), _ptr(part_lse), int(n_threads))
     if rc != 0:
         raise ValueError(f"oracle_verify_attn_f64kv rejected its arguments (rc={rc})")
+    return dict(out=out, lse=lse, part_o=part_o[:S], part_lse=part_lse[:S], ranges=list(split_ranges))
+
+
+def verify_attn_tree_decoded(q_bits, k_dec, v_dec, base: int, masks, n_nodes: int, sink, scale: float,
+                             window: int = 0, n_splits: int = 0, split_ranges=None, n_threads: int = 1):
+    """FP64 tree verify attention ("Qwen3.8-27B on one RTX 4090", section "More tokens per round: verify
+    trees") over a decoded (float64) linear history k_dec, v_dec [ctx, 128]: the nodes at base ..
+    base + n_nodes - 1 under their ancestor-or-self masks.  Arguments and result as oracle.verify_attn_tree."""
+    q = np.ascontiguousarray(np.asarray(q_bits).view(np.uint16) if np.asarray(q_bits).dtype == np.int16
+                             else np.asarray(q_bits, dtype=np.uint16))
+    kd = np.ascontiguousarray(np.asarray(k_dec, dtype=np.float64))
+    vd = np.ascontiguousarray(np.asarray(v_dec, dtype=np.float64))
+    n_rows = q.shape[0]
+    assert q.shape == (n_rows, Q_HEADS, HEAD_DIM) and kd.shape == vd.shape and kd.shape[1] == HEAD_DIM
+    tree = np.zeros(1 + n_rows, dtype=np.int32)
+    tree[0] = base
+    tree[1:1 + n_nodes] = np.asarray(masks, dtype=np.int64)[:n_nodes]
+    sk = None if sink is None else np.ascontiguousarray(np.asarray(sink, dtype=np.float64))
+    if n_splits > 0 and split_ranges is None:
+        lo, hi = tree_extent(base, tree[1:], n_nodes, window)
+        split_ranges = split_position_ranges(lo, hi, n_splits)
+    split_ranges = split_ranges or []
+    S = len(split_ranges)
+    sa = np.ascontiguousarray(np.array([a for a, _ in split_ranges] or [0], dtype=np.int64))
+    sb = np.ascontiguousarray(np.array([b for _, b in split_ranges] or [0], dtype=np.int64))
+    out = np.zeros((n_rows, Q_HEADS, HEAD_DIM))
+    lse = np.zeros((n_rows, Q_HEADS))
+    part_o = np.zeros((max(S, 1), n_rows, Q_HEADS, HEAD_DIM))
+    part_lse = np.zeros((max(S, 1), n_rows, Q_HEADS))
+    rc = _load().oracle_verify_attn_tree_f64kv(_ptr(q), _ptr(kd), _ptr(vd), kd.shape[0], _ptr(tree), n_rows,
+                                               n_nodes, _ptr(sk), float(scale), int(window), S, _ptr(sa), _ptr(sb),
+                                               _ptr(out), _ptr(lse), _ptr(part_o), _ptr(part_lse), int(n_threads))
+    if rc != 0:
+        raise ValueError(f"oracle_verify_attn_tree_f64kv rejected its arguments (rc={rc})")
     return dict(out=out, lse=lse, part_o=part_o[:S], part_lse=part_lse[:S], ranges=list(split_ranges))

@@ -269,10 +269,10 @@ int oracle_verify_attn_f64kv(const uint16_t *q, const double *kd, const double *
  *   tree  [1 + n_rows] int32: tree[0] = base, tree[1 + i] = ancestor-or-self mask of node i (i < n_nodes)
  * Other arguments as oracle_verify_attn; rows past n_nodes are padding.
  */
-int oracle_verify_attn_tree(const uint16_t *q, const uint16_t *kh, const uint16_t *vh, int64_t ctx,
-                            const int32_t *tree, int n_rows, int n_nodes, const double *sink, double scale,
-                            int64_t window, int n_splits, const int64_t *split_a, const int64_t *split_b,
-                            double *out, double *lse, double *part_o, double *part_lse, int n_threads)
+static int tree_run(const uint16_t *q, const uint16_t *kh, const uint16_t *vh, const double *kd,
+                    const double *vd, int64_t ctx, const int32_t *tree, int n_rows, int n_nodes, const double *sink,
+                    double scale, int64_t window, int n_splits, const int64_t *split_a, const int64_t *split_b,
+                    double *out, double *lse, double *part_o, double *part_lse, int n_threads)
 {
     if (!tree || n_rows < 1 || n_rows > 64 || n_nodes < 0 || n_nodes > n_rows || n_nodes > 31 || tree[0] < 0)
         return -1;
@@ -280,8 +280,34 @@ int oracle_verify_attn_tree(const uint16_t *q, const uint16_t *kh, const uint16_
         if (!((tree[1 + i] >> i) & 1) || (tree[1 + i] >> n_nodes) != 0 || tree[1 + i] < 0) return -1;
     int32_t last[64];
     for (int r = 0; r < n_rows; ++r) last[r] = tree[0] + (n_nodes > 0 ? n_nodes - 1 : 0);
-    return run(q, kh, vh, NULL, NULL, ctx, last, n_rows, n_nodes, sink, scale, window, tree, n_splits, split_a,
+    return run(q, kh, vh, kd, vd, ctx, last, n_rows, n_nodes, sink, scale, window, tree, n_splits, split_a,
                split_b, out, lse, part_o, part_lse, n_threads);
+}
+
+int oracle_verify_attn_tree(const uint16_t *q, const uint16_t *kh, const uint16_t *vh, int64_t ctx,
+                            const int32_t *tree, int n_rows, int n_nodes, const double *sink, double scale,
+                            int64_t window, int n_splits, const int64_t *split_a, const int64_t *split_b,
+                            double *out, double *lse, double *part_o, double *part_lse, int n_threads)
+{
+    if (!kh || !vh) return -1;
+    return tree_run(q, kh, vh, NULL, NULL, ctx, tree, n_rows, n_nodes, sink, scale, window, n_splits, split_a,
+                    split_b, out, lse, part_o, part_lse, n_threads);
+}
+
+/*
+ * The tree verification above over a history given as doubles (kd, vd [ctx][128]), as
+ * oracle_verify_attn_f64kv is to oracle_verify_attn: the quantised cache's decoded keys and values
+ * ("Qwen3.8-27B on one RTX 4090": the verify trees of "More tokens per round: verify trees" read the
+ * cache of "A cheaper cache and state").
+ */
+int oracle_verify_attn_tree_f64kv(const uint16_t *q, const double *kd, const double *vd, int64_t ctx,
+                                  const int32_t *tree, int n_rows, int n_nodes, const double *sink, double scale,
+                                  int64_t window, int n_splits, const int64_t *split_a, const int64_t *split_b,
+                                  double *out, double *lse, double *part_o, double *part_lse, int n_threads)
+{
+    if (!kd || !vd) return -1;
+    return tree_run(q, NULL, NULL, kd, vd, ctx, tree, n_rows, n_nodes, sink, scale, window, n_splits, split_a,
+                    split_b, out, lse, part_o, part_lse, n_threads);
 }
 
 static int run(const uint16_t *q, const uint16_t *kh, const uint16_t *vh, const double *kd, const double *vd,

@@ -6,11 +6,13 @@
 
 #include "va_internal.cuh"
 
-namespace {
+namespace va {
 
+namespace {
 constexpr int kMaxDevices = 64;
 int g_sm_count[kMaxDevices];  // 0 = not queried yet
 std::mutex g_mu;
+}  // namespace
 
 int device_sm_count() {
     int dev = 0;
@@ -29,6 +31,12 @@ int device_sm_count() {
     }
     return g_sm_count[dev];
 }
+
+}  // namespace va
+
+namespace {
+
+using va::device_sm_count;
 
 va_status from_cuda(cudaError_t e) { return e == cudaSuccess ? VA_OK : VA_CUDA_ERROR; }
 

@@ -19,6 +19,9 @@
 //     K codes once QK has read them.  The running sums use p itself.
 //   * The V code stage is released as soon as it is widened; the fp16 V buffer is double-buffered and
 //     reused once the PV two tiles back has completed.
+//   * Draft trees ("Qwen3.8-27B on one RTX 4090", section "More tokens per round: verify trees", over the
+//     cache of "A cheaper cache and state"): as in the bf16 kernel, each node's ancestor mask replaces the
+//     causal tail in the node region, and up to 16 nodes run as two groups of 8 rows (grid.y).
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -83,7 +86,11 @@ struct Misc {
     float qsig[kMaxM];                // power-of-two scale of each rotated q row
     float qinv[kMaxM];
     long long row_lo[kMaxRows], row_hi[kMaxRows];
+    long long tree_base;              // tree calls: slot of node 0; chain calls: no node region (LLONG_MAX)
+    unsigned row_anc[kMaxRows];       // ancestor-or-self mask of each row of this CTA's group
     int pos[kMaxRows];
+    int anc[kMaxNodes];               // tree calls: every node's mask
+    int base;
     __align__(16) float kscale[kNK][128];
     __align__(16) float vscale[kNV][128];
 };
@@ -171,9 +178,13 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
     unsigned char* base = smem_raw + (base_s - raw_s);
     Misc& ms = *reinterpret_cast<Misc*>(base + kOffMisc);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int split = blockIdx.x;
-    const int M = a.n_rows * kH;
-    const int ML = a.n_live * kH;
+    const int split = blockIdx.x, group = blockIdx.y;
+    const bool is_tree = a.tree != nullptr;
+    // rows of this CTA: group g holds rows 8 g .. 8 g + 7 (one group for chains)
+    const int n_live_g = is_tree ? min(max(a.n_live - kMaxRows * group, 0), kMaxRows) : a.n_live;
+    const int M_all = a.n_rows * kH;
+    const int M = min(kMaxM, M_all - kMaxM * group);
+    const int ML = n_live_g * kH;
     auto bar = [](const uint64_t& b) { return ptx::smem_u32(&b); };
 
     // ---------------------------------------------------------------- set-up without global memory
@@ -243,20 +254,37 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
     if (tid == 0) {
         const uint64_t keep = ptx::policy_evict_last();
         ptx::mbar_arrive_expect_tx(bar(ms.q_tma), kMaxM * kD * 2);
-        ptx::tma_load_2d_hint(base_s + kOffQStage, &tmq, 0, 0, bar(ms.q_tma), keep);
-        ptx::tma_load_2d_hint(base_s + kOffQStage + kQHalf16, &tmq, 64, 0, bar(ms.q_tma), keep);
+        ptx::tma_load_2d_hint(base_s + kOffQStage, &tmq, 0, kMaxM * group, bar(ms.q_tma), keep);
+        ptx::tma_load_2d_hint(base_s + kOffQStage + kQHalf16, &tmq, 64, kMaxM * group, bar(ms.q_tma), keep);
     }
-    if (warp == 0 && lane < a.n_live) ms.pos[lane] = ptx::ld_int_policy(a.pos + lane, ptx::policy_evict_last());
+    // the positions (or the tree): one request per CTA, shared through shared memory
+    if (warp == 0) {
+        if (!is_tree) {
+            if (lane < a.n_live) ms.pos[lane] = ptx::ld_int_policy(a.pos + lane, ptx::policy_evict_last());
+        } else if (lane <= a.n_live) {
+            const int w = ptx::ld_int_policy(a.tree + lane, ptx::policy_evict_last());
+            if (lane == 0) ms.base = w;
+            else ms.anc[lane - 1] = w;
+        }
+    }
     __syncthreads();
     int row_pos[kMaxRows];
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) row_pos[r] = (r < a.n_live) ? ms.pos[r] : 0;
-    const Plan P = make_plan(row_pos, a.n_live, a.window, a.slots, a.n_splits, split);
-    if (P.status && split == 0 && tid == 0 && a.dev_status) atomicOr(a.dev_status, P.status);
-    const int n64 = P.status ? 0 : (int)(P.t1 - P.t0);
+    for (int r = 0; r < kMaxRows; ++r) row_pos[r] = (!is_tree && r < a.n_live) ? ms.pos[r] : 0;
+    Plan P;
+    if (!is_tree) {
+        P = make_plan(row_pos, a.n_live, a.window, a.slots, a.n_splits, split);
+    } else {
+        int anc[kMaxNodes];
+#pragma unroll
+        for (int i = 0; i < kMaxNodes; ++i) anc[i] = (i < a.n_live) ? ms.anc[i] : 0;
+        P = make_tree_plan(ms.base, anc, a.n_live, a.window, a.slots, a.n_splits, split);
+    }
+    if (P.status && split == 0 && group == 0 && tid == 0 && a.dev_status) atomicOr(a.dev_status, P.status);
+    const int n64 = (P.status || n_live_g == 0) ? 0 : (int)(P.t1 - P.t0);
     const int ntiles = (n64 + 1) >> 1;
-    float* part_o = a.part_o + (long long)split * M * kD;
-    float* part_lse = a.part_lse + (long long)split * M;
+    float* part_o = a.part_o + ((long long)split * M_all + kMaxM * group) * kD;
+    float* part_lse = a.part_lse + (long long)split * M_all + kMaxM * group;
     const long long own_lo = max(P.lo, P.t0 * kTile);
     const long long own_hi = min(P.hi, P.t1 * kTile);
 
@@ -293,18 +321,30 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
 
     if (ntiles > 0) {
         if (tid < kMaxRows) {
+            // row tid of this group: the positions it sees inside this split, [lo, hi), and its mask of
+            // the node region [tree_base, hi)
             long long lo = 0, hi = 0;
+            unsigned m = 0xFFFFFFFFu;
+            if (!is_tree) {
 #pragma unroll
-            for (int r = 0; r < kMaxRows; ++r) {
-                if (r == tid && r < a.n_live) {
-                    const long long p = row_pos[r];
-                    lo = max(a.window > 0 ? max(0LL, p - a.window + 1) : 0LL, own_lo);
-                    hi = min(p + 1, own_hi);
-                    if (hi < lo) hi = lo;
+                for (int r = 0; r < kMaxRows; ++r) {
+                    if (r == tid && r < a.n_live) {
+                        const long long p = row_pos[r];
+                        lo = max(a.window > 0 ? max(0LL, p - a.window + 1) : 0LL, own_lo);
+                        hi = min(p + 1, own_hi);
+                    }
                 }
+            } else if (tid < n_live_g) {
+                m = (unsigned)ms.anc[kMaxRows * group + tid];
+                const long long logical = (long long)ms.base + tree_depth((int)m);   // the node's own position
+                lo = max(a.window > 0 ? max(0LL, logical - a.window + 1) : 0LL, own_lo);
+                hi = min(P.hi, own_hi);
             }
+            if (hi < lo) hi = lo;
             ms.row_lo[tid] = lo;
             ms.row_hi[tid] = hi;
+            ms.row_anc[tid] = m;
+            if (tid == 0) ms.tree_base = is_tree ? (long long)ms.base : LLONG_MAX;
         }
         if (tid < kMaxM) ms.ref[tid] = tid < ML ? kRefInit : INFINITY;
     }
@@ -487,10 +527,11 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
             l[i] = 0.0f;
         }
         long long all_lo = own_lo, all_hi = own_hi;
-        for (int r = 0; r < a.n_live; ++r) {
+        for (int r = 0; r < n_live_g; ++r) {
             all_lo = max(all_lo, ms.row_lo[r]);
             all_hi = min(all_hi, ms.row_hi[r]);
         }
+        all_hi = min(all_hi, ms.tree_base);   // the node region of a tree is never interior
         for (int j = 0; j < ntiles; ++j) {
             const long long t = P.t0 + 2LL * j;
             const int nkeys = (t + 1 < P.t1) ? 128 : 64;
@@ -533,10 +574,17 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
             bool vis[kCols];
             {
                 bool rv[kMaxRows / 2];
+                if (interior) {
 #pragma unroll
-                for (int k = 0; k < kMaxRows / 2; ++k) {
-                    const int r = (kMaxRows / 2) * ch + k;
-                    rv[k] = interior ? (L < nkeys) : ((r < a.n_live) && kp >= ms.row_lo[r] && kp < ms.row_hi[r]);
+                    for (int k = 0; k < kMaxRows / 2; ++k) rv[k] = L < nkeys;
+                } else {
+                    const long long dk = kp - ms.tree_base;   // node index of key kp in a tree's node region
+#pragma unroll
+                    for (int k = 0; k < kMaxRows / 2; ++k) {
+                        const int r = (kMaxRows / 2) * ch + k;
+                        const bool in_mask = dk < 0 || (dk < 32 && ((ms.row_anc[r] >> (int)dk) & 1u));
+                        rv[k] = (r < n_live_g) && kp >= ms.row_lo[r] && kp < ms.row_hi[r] && in_mask;
+                    }
                 }
 #pragma unroll
                 for (int i = 0; i < kCols; ++i) vis[i] = rv[i / kH];
@@ -702,6 +750,7 @@ bool encode_codes_map(CUtensorMap* map, const void* base, int rows, int box_rows
 }  // namespace q8
 
 cudaError_t launch_attn_q8(const AttnArgs& a, const float* k_scale, const float* v_scale, cudaStream_t stream) {
+    if (a.n_groups < 1 || a.n_groups * kMaxRows < a.n_rows || (a.n_groups > 1 && !a.tree)) return cudaErrorInvalidValue;
     CUtensorMap tmq, tmk, tmv, tmk2, tmv2;
     if (!tc::encode_rows_map(&tmq, a.q, a.n_rows * kH, kMaxM) || !q8::encode_codes_map(&tmk, a.k, a.slots, 64) || !q8::encode_codes_map(&tmv, a.v, a.slots, 64) ||
         !q8::encode_codes_map(&tmk2, a.k, a.slots, 128) || !q8::encode_codes_map(&tmv2, a.v, a.slots, 128))
@@ -710,7 +759,7 @@ cudaError_t launch_attn_q8(const AttnArgs& a, const float* k_scale, const float*
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    pdl_config(&cfg, attr, dim3(a.n_splits), dim3(q8::kThreads), q8::kSmemBytes, stream);
+    pdl_config(&cfg, attr, dim3(a.n_splits, a.n_groups), dim3(q8::kThreads), q8::kSmemBytes, stream);
     e = cudaLaunchKernelEx(&cfg, q8::attn_q8_kernel, a, k_scale, v_scale, tmq, tmk, tmv, tmk2, tmv2);
     return e != cudaSuccess ? e : cudaGetLastError();
 }

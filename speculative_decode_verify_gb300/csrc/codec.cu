@@ -142,4 +142,39 @@ va_status verify_attn_q8(const va_bf16* q, int n_rows, int n_live, const uint8_t
     return VA_OK;
 }
 
+va_status verify_attn_q8_tree(const va_bf16* q, int n_rows, int n_nodes, const uint8_t* k_codes, const int8_t* v_codes,
+                              const float* k_scale, const float* v_scale, int slots, int window, const int32_t* tree,
+                              float scale, int n_splits, float* part_o, float* part_lse, int* splits_used,
+                              int32_t* dev_status, va_stream stream) {
+    using va::codec::aligned16;
+    if (!q || !k_codes || !v_codes || !k_scale || !v_scale || !tree || !part_o || !part_lse) return VA_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scale) || !aligned16(v_scale) ||
+        !aligned16(part_o) || !aligned16(part_lse))
+        return VA_INVALID_ARG;
+    if (n_rows < 1 || n_rows > VA_MAX_TREE_NODES || n_nodes < 0 || n_nodes > n_rows || slots < 1) return VA_INVALID_ARG;
+    if (!std::isfinite(scale) || window < 0 || n_splits < 0 || n_splits > VA_MAX_SPLITS) return VA_INVALID_ARG;
+    if (slots % VA_TILE != 0) return VA_UNSUPPORTED;
+    if (window > 0) {
+        if (window < n_nodes) return VA_UNSUPPORTED;   // every ancestor must lie inside every window
+        if ((long long)slots < (long long)window + (n_nodes > 0 ? n_nodes - 1 : 0)) return VA_RING_TOO_SMALL;
+    }
+    const int groups = (n_rows + VA_MAX_ROWS - 1) / VA_MAX_ROWS;
+    if (n_splits == 0) {
+        // the node groups share the SMs: at most one CTA per SM over all groups
+        const int sms = va::device_sm_count();
+        const int extent = window > 0 ? window + (n_nodes > 0 ? n_nodes - 1 : 0) : slots;
+        n_splits = va_auto_splits_for(extent, window, (sms > 0 ? sms : 148) / groups);
+    }
+    va::AttnArgs a;
+    a.q = q; a.k = reinterpret_cast<const uint16_t*>(k_codes); a.v = reinterpret_cast<const uint16_t*>(v_codes);
+    a.pos = nullptr; a.tree = tree;
+    a.part_o = part_o; a.part_lse = part_lse; a.dev_status = dev_status;
+    a.scale = scale; a.n_rows = n_rows; a.n_live = n_nodes; a.slots = slots; a.window = window;
+    a.n_splits = n_splits; a.n_groups = groups;
+    const cudaError_t e = va::launch_attn_q8(a, k_scale, v_scale, (cudaStream_t)stream);
+    if (e != cudaSuccess) return VA_CUDA_ERROR;
+    if (splits_used) *splits_used = n_splits;
+    return VA_OK;
+}
+
 }  // extern "C"

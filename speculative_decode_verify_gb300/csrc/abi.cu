@@ -8,6 +8,8 @@
 
 namespace va {
 
+int device_sm_count();   // also called by codec.cu
+
 namespace {
 constexpr int kMaxDevices = 64;
 int g_sm_count[kMaxDevices];  // 0 = not queried yet

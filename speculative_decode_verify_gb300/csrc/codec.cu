@@ -13,6 +13,7 @@
 namespace va {
 
 cudaError_t launch_attn_q8(const AttnArgs& a, const float* k_scale, const float* v_scale, cudaStream_t stream);
+int device_sm_count();   // abi.cu: multiprocessors of the current device (0 if the query fails)
 
 namespace codec {
 

@@ -117,9 +117,6 @@ __device__ __forceinline__ Plan make_tree_plan(int base, const int (&anc)[kMaxNo
     return P;
 }
 
-// Multiprocessors of the current device (queried once per device; 0 if the query fails).
-int device_sm_count();
-
 // Opt a kernel into `bytes` of dynamic shared memory on the current device, once per device
 // (so that a later launch under stream capture issues no attribute call).
 cudaError_t ensure_smem_attr(const void* kernel, int bytes);

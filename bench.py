@@ -72,6 +72,9 @@ def parse():
                     help="profiling aid: only top-k/top-p sampling launches (8 x 160,000 logits), 2 buffers")
     ap.add_argument("--q8-kernel-only", action="store_true",
                     help="profiling aid: only verify_attn_q8 launches (quantised 192K cache), over 2 caches")
+    ap.add_argument("--q8-tree-kernel-only", action="store_true",
+                    help="profiling aid: only verify_attn_q8_tree launches (16-node tree, quantised 192K cache), "
+                         "over 2 caches")
     ap.add_argument("--caches", type=int, default=5, help="distinct 192K caches to rotate (1..5)")
     ap.add_argument("--variant", default="", help="library build variant to load (A/B tuning aid)")
     ap.add_argument("--ctx", type=int, default=CTX, help="context of the --kernel-only runs")
@@ -723,18 +726,35 @@ def ours(args, dist: Dist):
         res["tree_accept_settle"] = {"nodes": 16, "us_per_call": graph_time([settle] * 16)}
         return res
 
-    if args.q8_kernel_only:
-        # the quantised-cache split kernel alone, back to back over two caches (for ncu captures)
+    if args.q8_kernel_only or args.q8_tree_kernel_only:
+        # the quantised-cache split kernel alone (chain or 16-node tree), back to back over two caches (for
+        # ncu captures)
         qs = q8_caches(2)
-        po = torch.empty(S, 8, 6, 128, dtype=torch.float32, device=dev)
-        pl = torch.empty(S, 8, 6, dtype=torch.float32, device=dev)
+        tree_mode = args.q8_tree_kernel_only
+        Sq = va.va_auto_splits_for(CAPACITY, 0, torch.cuda.get_device_properties(dev).multi_processor_count // 2) \
+            if tree_mode else S
+        rows = 16 if tree_mode else 8
+        po = torch.empty(Sq, rows, 6, 128, dtype=torch.float32, device=dev)
+        pl = torch.empty(Sq, rows, 6, dtype=torch.float32, device=dev)
+        for i, c in enumerate(qs):
+            tw = synth.make_tree(f"prof_q8tree{i}", 520 + i, base=0, n_nodes=16)
+            tree = tw.tree.clone()
+            tree[0] = CTX - 16
+            c["tree"], c["tq"] = tree.to(dev), synth.bits(tw.q).to(dev)
         with torch.cuda.stream(stream):
             def attn_q8(c):
-                st = L.verify_attn_q8(P(c["q"].data_ptr()), 8, c["n"], P(c["kc"].data_ptr()), P(c["vc"].data_ptr()),
-                                      P(c["ks"].data_ptr()), P(c["vs"].data_ptr()), CAPACITY, 0, P(c["pos"].data_ptr()),
-                                      ctypes.c_float(c["w"].scale), S, P(po.data_ptr()), P(pl.data_ptr()), None, None, sp)
+                if tree_mode:
+                    st = L.verify_attn_q8_tree(P(c["tq"].data_ptr()), 16, 16, P(c["kc"].data_ptr()),
+                                               P(c["vc"].data_ptr()), P(c["ks"].data_ptr()), P(c["vs"].data_ptr()),
+                                               CAPACITY, 0, P(c["tree"].data_ptr()), ctypes.c_float(c["w"].scale), Sq,
+                                               P(po.data_ptr()), P(pl.data_ptr()), None, None, sp)
+                else:
+                    st = L.verify_attn_q8(P(c["q"].data_ptr()), 8, c["n"], P(c["kc"].data_ptr()),
+                                          P(c["vc"].data_ptr()), P(c["ks"].data_ptr()), P(c["vs"].data_ptr()), CAPACITY,
+                                          0, P(c["pos"].data_ptr()), ctypes.c_float(c["w"].scale), Sq,
+                                          P(po.data_ptr()), P(pl.data_ptr()), None, None, sp)
                 if st:
-                    raise RuntimeError(f"verify_attn_q8 failed with status {st}")
+                    raise RuntimeError(f"quantised verify failed with status {st}")
             for _ in range(max(args.warmup, 1)):
                 for c in qs:
                     attn_q8(c)
@@ -746,8 +766,8 @@ def ours(args, dist: Dist):
             e1.record(stream)
             e1.synchronize()
         us = e0.elapsed_time(e1) * 1e3 / (args.steps * len(qs))
-        print(json.dumps({"kernel_only": "verify_attn_q8", "launches": args.steps * len(qs), "us_per_launch": us,
-                          "gbs": 264 * CTX / us / 1e3}))
+        print(json.dumps({"kernel_only": "verify_attn_q8_tree" if tree_mode else "verify_attn_q8",
+                          "launches": args.steps * len(qs), "us_per_launch": us, "gbs": 264 * CTX / us / 1e3}))
         return
 
     if args.kernel_only:

@@ -132,6 +132,28 @@ __device__ __forceinline__ void int8x4_to_half(uint32_t w, uint32_t& h01, uint32
     h23 = *reinterpret_cast<uint32_t*>(&hb);
 }
 
+// Packed fp32 pairs (one instruction for two IEEE round-to-nearest operations, each rounded as the scalar
+// operation would be).
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 r;
+    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n add.rn.f32x2 rd, ra, rb;\n"
+        " mov.b64 {%0, %1}, rd;\n}" : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 r;
+    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mul.rn.f32x2 rd, ra, rb;\n"
+        " mov.b64 {%0, %1}, rd;\n}" : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 r;
+    asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%6, %7};\n"
+        " fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(r.x), "=f"(r.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return r;
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     const __half2 v = __floats2half2_rn(lo, hi);
     uint32_t u;
@@ -600,7 +622,11 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
                 for (int t = 1; t < 3; ++t) {
                     ptx::tmem_ld24_wait(sc + t * kTermCols, y);
 #pragma unroll
-                    for (int i = 0; i < kCols; ++i) x[i] += y[i];
+                    for (int i = 0; i < kCols; i += 2) {
+                        const float2 s2 = add2(make_float2(x[i], x[i + 1]), make_float2(y[i], y[i + 1]));
+                        x[i] = s2.x;
+                        x[i + 1] = s2.y;
+                    }
                 }
             }
             ptx::tc_fence_before();
@@ -608,7 +634,11 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
             if (lane == 0) ptx::mbar_arrive(bar(ms.s_free[sb]));
             const float sk = ms.kscale[ks][L];
 #pragma unroll
-            for (int i = 0; i < kCols; ++i) x[i] *= sk;   // score = x * cq[i] in log2 units
+            for (int i = 0; i < kCols; i += 2) {   // score = x * cq[i] in log2 units
+                const float2 s2 = mul2(make_float2(x[i], x[i + 1]), make_float2(sk, sk));
+                x[i] = s2.x;
+                x[i + 1] = s2.y;
+            }
             if (j == 0) {
                 if (L == 0) {
 #pragma unroll
@@ -622,9 +652,12 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
             float p[kCols];
             float pmax = 0.0f;
 #pragma unroll
-            for (int i = 0; i < kCols; ++i) {
-                p[i] = vis[i] ? ptx::ex2(fmaf(x[i], cq[i], -ref[i])) : 0.0f;
-                pmax = fmaxf(pmax, p[i]);
+            for (int i = 0; i < kCols; i += 2) {
+                const float2 e2 = fma2(make_float2(x[i], x[i + 1]), make_float2(cq[i], cq[i + 1]),
+                                       make_float2(-ref[i], -ref[i + 1]));
+                p[i] = vis[i] ? ptx::ex2(e2.x) : 0.0f;
+                p[i + 1] = vis[i + 1] ? ptx::ex2(e2.y) : 0.0f;
+                pmax = fmaxf(pmax, fmaxf(p[i], p[i + 1]));
             }
             const unsigned want = __any_sync(0xffffffffu, !(pmax <= kThresh));
             if (lane == 0) ms.vote[j & 1][sw] = want ? 1 : 0;
@@ -672,13 +705,19 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
                 }
             }
 #pragma unroll
-            for (int i = 0; i < kCols; ++i) l[i] += p[i];
+            for (int i = 0; i < kCols; i += 2) {
+                const float2 s2 = add2(make_float2(l[i], l[i + 1]), make_float2(p[i], p[i + 1]));
+                l[i] = s2.x;
+                l[i + 1] = s2.y;
+            }
 
             // P' = p * v_scale as fp16, over this tile's K codes (QK(j) has read them)
             uint32_t pw[kCols / 2];
 #pragma unroll
-            for (int i = 0; i < kCols / 2; ++i)
-                pw[i] = own ? pack_half2(p[2 * i] * sv, p[2 * i + 1] * sv) : 0u;
+            for (int i = 0; i < kCols / 2; ++i) {
+                const float2 s2 = mul2(make_float2(p[2 * i], p[2 * i + 1]), make_float2(sv, sv));
+                pw[i] = own ? pack_half2(s2.x, s2.y) : 0u;
+            }
             {
                 const uint32_t roff = kOffK + (uint32_t)ks * kStage + (uint32_t)(L >> 3) * 1024u + (uint32_t)(L & 7) * 128u;
 #pragma unroll

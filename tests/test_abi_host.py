@@ -210,3 +210,83 @@ def test_accept_and_settle_argument_checks(L):
         bad = list(s)
         bad[i] = v
         assert L.va_tree_accept_settle(*bad) == va.VA_INVALID_ARG, (i, v)
+
+
+def _step(L, **kw):
+    a = dict(q=FAKE, kn=FAKE, vn=FAKE, n_rows=8, n_live=8, k=FAKE, v=FAKE, slots=4160, W=4096, pos=FAKE, sink=None,
+             scale=0.088, S=4, ws=FAKE, out=FAKE)
+    a.update(kw)
+    return L.verify_attn_step(a["q"], a["kn"], a["vn"], a["n_rows"], a["n_live"], a["k"], a["v"], a["slots"], a["W"],
+                              a["pos"], a["sink"], a["scale"], a["S"], a["ws"], a["out"], None, None, None, None)
+
+
+@pytest.mark.parametrize("kw", [dict(out=None), dict(out=ctypes.c_void_p(0x1002)), dict(kn=None), dict(vn=None),
+                                dict(kn=ctypes.c_void_p(0x1004)), dict(W=-1), dict(S=-1), dict(S=4097), dict(ws=None),
+                                dict(q=None), dict(k=None), dict(pos=None), dict(n_rows=0), dict(n_rows=9),
+                                dict(n_live=9), dict(n_live=-1), dict(slots=0), dict(scale=float("nan"))])
+def test_step_rejects_bad_arguments(L, kw):
+    assert _step(L, **kw) == va.VA_INVALID_ARG
+
+
+def test_step_ring_checks(L):
+    assert _step(L, slots=4100) == va.VA_UNSUPPORTED            # a ring must hold whole 64-position tiles
+    assert _step(L, slots=4096) == va.VA_RING_TOO_SMALL         # needs W + n_live - 1 slots
+    assert _step(L, slots=4160, W=4160 - 6) == va.VA_RING_TOO_SMALL
+
+
+def _q8(L, **kw):
+    a = dict(q=FAKE, n_rows=8, n_live=8, kc=FAKE, vc=FAKE, ks=FAKE, vs=FAKE, slots=4160, W=4096, pos=FAKE,
+             scale=0.088, S=4, po=FAKE, pl=FAKE)
+    a.update(kw)
+    return L.verify_attn_q8(a["q"], a["n_rows"], a["n_live"], a["kc"], a["vc"], a["ks"], a["vs"], a["slots"], a["W"],
+                            a["pos"], a["scale"], a["S"], a["po"], a["pl"], None, None, None)
+
+
+@pytest.mark.parametrize("kw", [dict(q=None), dict(kc=None), dict(vc=None), dict(ks=None), dict(vs=None),
+                                dict(pos=None), dict(po=None), dict(pl=None), dict(ks=ctypes.c_void_p(0x1004)),
+                                dict(n_rows=0), dict(n_rows=9), dict(n_live=9), dict(n_live=-1), dict(slots=0),
+                                dict(W=-1), dict(S=-1), dict(S=4097), dict(scale=float("inf"))])
+def test_q8_rejects_bad_arguments(L, kw):
+    assert _q8(L, **kw) == va.VA_INVALID_ARG
+
+
+def test_q8_ring_checks(L):
+    assert _q8(L, slots=4100) == va.VA_UNSUPPORTED
+    assert _q8(L, slots=4100, W=0) == va.VA_UNSUPPORTED           # the quantised cache is tiled in 64 rows
+    assert _q8(L, slots=4096) == va.VA_RING_TOO_SMALL
+
+
+def _q8_tree(L, **kw):
+    a = dict(q=FAKE, n_rows=16, n_nodes=16, kc=FAKE, vc=FAKE, ks=FAKE, vs=FAKE, slots=4160, W=4096, tree=FAKE,
+             scale=0.088, S=4, po=FAKE, pl=FAKE)
+    a.update(kw)
+    return L.verify_attn_q8_tree(a["q"], a["n_rows"], a["n_nodes"], a["kc"], a["vc"], a["ks"], a["vs"], a["slots"],
+                                 a["W"], a["tree"], a["scale"], a["S"], a["po"], a["pl"], None, None, None)
+
+
+@pytest.mark.parametrize("kw", [dict(q=None), dict(tree=None), dict(kc=None), dict(vs=None), dict(po=None),
+                                dict(n_rows=0), dict(n_rows=17), dict(n_nodes=-1), dict(n_nodes=17),
+                                dict(n_rows=8, n_nodes=9), dict(slots=0), dict(W=-1), dict(S=-1), dict(S=4097),
+                                dict(scale=float("nan")), dict(vc=ctypes.c_void_p(0x1008))])
+def test_q8_tree_rejects_bad_arguments(L, kw):
+    assert _q8_tree(L, **kw) == va.VA_INVALID_ARG
+
+
+def test_q8_tree_window_and_ring_checks(L):
+    assert _q8_tree(L, W=15) == va.VA_UNSUPPORTED            # a window shorter than the tree
+    assert _q8_tree(L, slots=4100) == va.VA_UNSUPPORTED      # not a multiple of 64
+    assert _q8_tree(L, slots=4100, W=0) == va.VA_UNSUPPORTED
+    assert _q8_tree(L, slots=4096) == va.VA_RING_TOO_SMALL   # needs W + 15 slots
+
+
+def test_q8_append_argument_checks(L):
+    def call(n=4, kn=FAKE, kc=FAKE, ks=FAKE, slots=4160, pos=FAKE):
+        return L.kv_ring_append_q8(kn, FAKE, n, kc, FAKE, ks, FAKE, slots, pos, None, None)
+    assert call(n=-1) == va.VA_INVALID_ARG
+    assert call(n=16777217) == va.VA_INVALID_ARG
+    assert call(slots=0) == va.VA_INVALID_ARG
+    assert call(slots=100) == va.VA_UNSUPPORTED
+    assert call(kn=None) == va.VA_INVALID_ARG
+    assert call(pos=None) == va.VA_INVALID_ARG
+    assert call(ks=ctypes.c_void_p(0x1004)) == va.VA_INVALID_ARG
+    assert call(n=0, kn=None, kc=None, ks=None, pos=None) == va.VA_OK   # nothing to encode, nothing launched

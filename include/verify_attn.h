@@ -273,6 +273,21 @@ VA_API va_status verify_attn_full_noalloc(const va_bf16 *q, int n_rows, int n_li
                                           const float *sink, va_bf16 *out, float *out_lse,
                                           int *splits_used, int32_t *dev_status, va_stream stream);
 
+/*
+ * va_selftest_bounded_wait - failure detection without a fault.  Every wait in the library's kernels
+ * (on a TMA arrival, an MMA completion, another warp) gives up after a time limit, or at once when a
+ * warp of the same CTA has raised the CTA's abort flag, and reports VA_DEV_TIMEOUT.  This call runs that
+ * wait routine on a shared-memory barrier that nothing completes (one CTA of 64 threads).
+ *   limit_ns        1 .. VA_SELFTEST_MAX_WAIT_NS: the wait's limit
+ *   abort_after_ns  0 (no abort) or <= limit_ns: a second warp raises the abort flag after this long
+ *   dev_status      optional device int32: VA_DEV_TIMEOUT is OR-ed in when the wait gives up
+ *   elapsed_ns      optional device uint64: how long the wait lasted (globaltimer)
+ * Returns VA_OK, VA_INVALID_ARG or VA_CUDA_ERROR.  The context stays usable afterwards.
+ */
+#define VA_SELFTEST_MAX_WAIT_NS 1000000000ull
+VA_API va_status va_selftest_bounded_wait(unsigned long long limit_ns, unsigned long long abort_after_ns,
+                                          int32_t *dev_status, unsigned long long *elapsed_ns, va_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

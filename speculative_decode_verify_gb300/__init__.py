@@ -18,7 +18,7 @@ __all__ = [
     "VerifyAttnError", "lib", "lib_path", "kv_ring_append", "verify_attn_full", "verify_attn_swa",
     "attn_split_combine", "verify_attn_tree", "verify_attn_full_noalloc", "va_sample_workspace_bytes",
     "va_sample_topk_topp", "va_accept_chain", "va_tree_accept_settle", "kv_ring_append_q8", "verify_attn_q8",
-    "verify_attn_q8_tree", "verify_attn_step", "SAMPLE_MAX_K", "SAMPLE_TILE",
+    "verify_attn_q8_tree", "verify_attn_step", "va_selftest_bounded_wait", "SAMPLE_MAX_K", "SAMPLE_TILE",
     "SAMPLE_MAX_VOCAB", "NOALLOC_MAX_SPLITS", "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string",
     "HEAD_DIM", "Q_HEADS", "MAX_ROWS", "TILE", "MAX_SPLITS", "MAX_TREE_NODES", "EXPORTS",
     "VA_OK", "VA_INVALID_ARG", "VA_UNSUPPORTED", "VA_RING_TOO_SMALL", "VA_CUDA_ERROR",
@@ -29,7 +29,8 @@ VA_OK, VA_INVALID_ARG, VA_UNSUPPORTED, VA_RING_TOO_SMALL, VA_CUDA_ERROR = 0, 1, 
 EXPORTS = ("kv_ring_append", "verify_attn_full", "verify_attn_swa", "verify_attn_tree", "attn_split_combine",
            "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string",
            "verify_attn_full_noalloc", "va_sample_workspace_bytes", "va_sample_topk_topp", "va_accept_chain",
-           "va_tree_accept_settle", "kv_ring_append_q8", "verify_attn_q8", "verify_attn_q8_tree", "verify_attn_step")
+           "va_tree_accept_settle", "kv_ring_append_q8", "verify_attn_q8", "verify_attn_q8_tree", "verify_attn_step",
+           "va_selftest_bounded_wait")
 NOALLOC_MAX_SPLITS = 160
 SAMPLE_MAX_K, SAMPLE_TILE, SAMPLE_MAX_VOCAB = 32, 8192, 262144
 
@@ -80,6 +81,8 @@ def lib(variant: str = "") -> ctypes.CDLL:
             getattr(L, fn).restype = i
         L.verify_attn_step.argtypes = [p, p, p, i, i, p, p, i, i, p, p, f, i, p, p, p, ctypes.POINTER(i), p, p]
         L.verify_attn_step.restype = i
+        L.va_selftest_bounded_wait.argtypes = [ctypes.c_ulonglong, ctypes.c_ulonglong, p, p, p]
+        L.va_selftest_bounded_wait.restype = i
         L.va_workspace_bytes.argtypes = [i]
         L.va_workspace_bytes.restype = ctypes.c_size_t
         L.va_auto_splits.argtypes = [i, i]
@@ -278,3 +281,12 @@ def verify_attn_q8_tree(q, n_nodes: int, k_codes, v_codes, k_scale, v_scale, tre
                                           ctypes.byref(used), _ptr(dev_status), _stream(stream))
     _check("verify_attn_q8_tree", st)
     return used.value
+
+
+# ----------------------------------------------------------------------------- self-test
+def va_selftest_bounded_wait(limit_ns: int, abort_after_ns: int = 0, dev_status=None, elapsed_ns=None, stream=None,
+                             variant: str = "") -> None:
+    """Run the kernels' bounded wait on a barrier nothing completes (see include/verify_attn.h)."""
+    st = lib(variant).va_selftest_bounded_wait(int(limit_ns), int(abort_after_ns), _ptr(dev_status),
+                                               _ptr(elapsed_ns), _stream(stream))
+    _check("va_selftest_bounded_wait", st)

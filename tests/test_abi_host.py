@@ -290,3 +290,9 @@ def test_q8_append_argument_checks(L):
     assert call(pos=None) == va.VA_INVALID_ARG
     assert call(ks=ctypes.c_void_p(0x1004)) == va.VA_INVALID_ARG
     assert call(n=0, kn=None, kc=None, ks=None, pos=None) == va.VA_OK   # nothing to encode, nothing launched
+
+
+def test_bounded_wait_selftest_argument_checks(L):
+    assert L.va_selftest_bounded_wait(0, 0, None, None, None) == va.VA_INVALID_ARG
+    assert L.va_selftest_bounded_wait(1_000_000_001, 0, None, None, None) == va.VA_INVALID_ARG
+    assert L.va_selftest_bounded_wait(1_000_000, 1_000_001, None, None, None) == va.VA_INVALID_ARG

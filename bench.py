@@ -370,11 +370,13 @@ def ours(args, dist: Dist):
         for c in calls:
             launch_call(c)
 
-    def sweep_points(ctx, window, reps=200):
+    def sweep_points(ctx, window, reps=100, per_graph=8):
         """us per call and algorithmic GB/s of one verify call (verify_attn_step with the library's split
-        choice, graph replay) at this context for n_live 4..8; two caches alternate so K/V are read cold
-        when they exceed L2.  The caches hold the whole history, so every n_live uses the same ones (the
-        append rewrites the live rows with their own values)."""
+        choice) at this context for n_live 4..8; two caches alternate so K/V are read cold when they exceed
+        L2.  One CUDA graph holds 2 x per_graph calls, as consecutive layers of a decode step would: a graph
+        of only two calls adds the device's per-graph launch gap (~3 us) to every other call.  The caches
+        hold the whole history, so every n_live uses the same ones (the append rewrites the live rows with
+        their own values)."""
         ws = []
         for rep in range(2):
             w = synth.make(f"sweep{ctx}", 900 + rep, ctx=ctx, n_live=8, window=window,
@@ -415,8 +417,9 @@ def ours(args, dist: Dist):
                         one(c)
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=stream):
-                    for c in ws:
-                        one(c)
+                    for _ in range(per_graph):
+                        for c in ws:
+                            one(c)
                 g.replay()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
@@ -424,7 +427,7 @@ def ours(args, dist: Dist):
                     g.replay()
                 e1.record(stream)
                 e1.synchronize()
-            us = e0.elapsed_time(e1) * 1e3 / (reps * 2)
+            us = e0.elapsed_time(e1) * 1e3 / (reps * 2 * per_graph)
             hi = ctx
             lo = max(0, ctx - n - window + 1) if window else 0
             nbytes = 512 * (hi - lo) + Q_BYTES + OUT_BYTES + 2 * 512 * n + 24

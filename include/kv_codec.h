@@ -34,7 +34,9 @@ extern "C" {
  *   n_live        0..VA_Q8_MAX_APPEND: the verify rows of a step, or a whole prefill history at once
  *   k_codes, v_codes  device uint8 / int8 [slots][128]; k_scale, v_scale device float [slots]
  *   slots         a multiple of 64 (else VA_UNSUPPORTED)
- *   pos           device int32 [>= n_live]; dev_status: VA_DEV_NEGATIVE_POS (the row is not written)
+ *   pos           device int32 [>= n_live]; dev_status: VA_DEV_NEGATIVE_POS (the row is not written).
+ *                 A row whose slot the next row also writes is skipped, so adjacent rows that share a slot
+ *                 land as if written in row order (rows that share a slot must be adjacent).
  * Returns VA_OK, VA_INVALID_ARG, VA_UNSUPPORTED or VA_CUDA_ERROR.
  */
 VA_API va_status kv_ring_append_q8(const va_bf16 *k_new, const va_bf16 *v_new, int n_live, uint8_t *k_codes,
@@ -52,6 +54,29 @@ VA_API va_status verify_attn_q8(const va_bf16 *q, int n_rows, int n_live, const 
                                 const int8_t *v_codes, const float *k_scale, const float *v_scale, int slots,
                                 int window, const int32_t *pos, float scale, int n_splits, float *part_o,
                                 float *part_lse, int *splits_used, int32_t *dev_status, va_stream stream);
+
+/*
+ * verify_attn_q8_step - a whole verify call over the quantised cache in one call: kv_ring_append_q8 of the
+ * live rows, verify_attn_q8, then attn_split_combine, on the stream in that order (three launches, each
+ * waiting for the previous one by programmatic dependent launch; capturable in a CUDA graph).  Source as
+ * verify_attn_q8 and kv_ring_append_q8.  (Coding the live rows inside the split kernel, as verify_attn_step
+ * does for the bf16 cache, measured no faster: the small append launch is hidden behind the split kernel's
+ * start.)
+ *   q, n_rows, n_live, k_codes, v_codes, k_scale, v_scale, slots, window, pos, scale, n_splits
+ *                 as verify_attn_q8 (the codes and scales are updated in place)
+ *   k_new, v_new  device [n_live][128] bf16, 16-byte aligned: the live rows' new K and V
+ *   sink          device float [6] or NULL, as attn_split_combine
+ *   workspace     device float, 16-byte aligned, va_workspace_bytes(n_splits) bytes, laid out as for
+ *                 verify_attn_step
+ *   out, out_lse  as attn_split_combine (n_rows, n_live)
+ *   splits_used   optional HOST int; dev_status optional device int32 (the bits of the two calls)
+ * Returns VA_OK, VA_INVALID_ARG, VA_UNSUPPORTED, VA_RING_TOO_SMALL or VA_CUDA_ERROR.
+ */
+VA_API va_status verify_attn_q8_step(const va_bf16 *q, const va_bf16 *k_new, const va_bf16 *v_new, int n_rows,
+                                     int n_live, uint8_t *k_codes, int8_t *v_codes, float *k_scale, float *v_scale,
+                                     int slots, int window, const int32_t *pos, const float *sink, float scale,
+                                     int n_splits, float *workspace, va_bf16 *out, float *out_lse, int *splits_used,
+                                     int32_t *dev_status, va_stream stream);
 
 /*
  * verify_attn_q8_tree - verify attention of a draft TREE over the quantised cache.

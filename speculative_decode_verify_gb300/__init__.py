@@ -18,7 +18,7 @@ __all__ = [
     "VerifyAttnError", "lib", "lib_path", "kv_ring_append", "verify_attn_full", "verify_attn_swa",
     "attn_split_combine", "verify_attn_tree", "verify_attn_full_noalloc", "va_sample_workspace_bytes",
     "va_sample_topk_topp", "va_accept_chain", "va_tree_accept_settle", "kv_ring_append_q8", "verify_attn_q8",
-    "verify_attn_q8_tree", "verify_attn_step", "va_selftest_bounded_wait", "SAMPLE_MAX_K", "SAMPLE_TILE",
+    "verify_attn_q8_tree", "verify_attn_q8_step", "verify_attn_step", "va_selftest_bounded_wait", "SAMPLE_MAX_K", "SAMPLE_TILE",
     "SAMPLE_MAX_VOCAB", "NOALLOC_MAX_SPLITS", "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string",
     "HEAD_DIM", "Q_HEADS", "MAX_ROWS", "TILE", "MAX_SPLITS", "MAX_TREE_NODES", "EXPORTS",
     "VA_OK", "VA_INVALID_ARG", "VA_UNSUPPORTED", "VA_RING_TOO_SMALL", "VA_CUDA_ERROR",
@@ -29,8 +29,8 @@ VA_OK, VA_INVALID_ARG, VA_UNSUPPORTED, VA_RING_TOO_SMALL, VA_CUDA_ERROR = 0, 1, 
 EXPORTS = ("kv_ring_append", "verify_attn_full", "verify_attn_swa", "verify_attn_tree", "attn_split_combine",
            "va_workspace_bytes", "va_auto_splits", "va_auto_splits_for", "va_status_string",
            "verify_attn_full_noalloc", "va_sample_workspace_bytes", "va_sample_topk_topp", "va_accept_chain",
-           "va_tree_accept_settle", "kv_ring_append_q8", "verify_attn_q8", "verify_attn_q8_tree", "verify_attn_step",
-           "va_selftest_bounded_wait")
+           "va_tree_accept_settle", "kv_ring_append_q8", "verify_attn_q8", "verify_attn_q8_tree", "verify_attn_q8_step",
+           "verify_attn_step", "va_selftest_bounded_wait")
 NOALLOC_MAX_SPLITS = 160
 SAMPLE_MAX_K, SAMPLE_TILE, SAMPLE_MAX_VOCAB = 32, 8192, 262144
 
@@ -76,8 +76,10 @@ def lib(variant: str = "") -> ctypes.CDLL:
         L.kv_ring_append_q8.argtypes = [p, p, i, p, p, p, p, i, p, p, p]
         L.verify_attn_q8.argtypes = [p, i, i, p, p, p, p, i, i, p, f, i, p, p, ctypes.POINTER(i), p, p]
         L.verify_attn_q8_tree.argtypes = [p, i, i, p, p, p, p, i, i, p, f, i, p, p, ctypes.POINTER(i), p, p]
+        L.verify_attn_q8_step.argtypes = [p, p, p, i, i, p, p, p, p, i, i, p, p, f, i, p, p, p, ctypes.POINTER(i),
+                                          p, p]
         for fn in ("va_sample_topk_topp", "va_accept_chain", "va_tree_accept_settle", "kv_ring_append_q8",
-                   "verify_attn_q8", "verify_attn_q8_tree"):
+                   "verify_attn_q8", "verify_attn_q8_tree", "verify_attn_q8_step"):
             getattr(L, fn).restype = i
         L.verify_attn_step.argtypes = [p, p, p, i, i, p, p, i, i, p, p, f, i, p, p, p, ctypes.POINTER(i), p, p]
         L.verify_attn_step.restype = i
@@ -280,6 +282,21 @@ def verify_attn_q8_tree(q, n_nodes: int, k_codes, v_codes, k_scale, v_scale, tre
                                           _ptr(tree), float(scale), int(n_splits), _ptr(part_o), _ptr(part_lse),
                                           ctypes.byref(used), _ptr(dev_status), _stream(stream))
     _check("verify_attn_q8_tree", st)
+    return used.value
+
+
+def verify_attn_q8_step(q, k_new, v_new, n_live: int, k_codes, v_codes, k_scale, v_scale, pos, scale: float, sink,
+                        workspace, out, out_lse=None, window: int = 0, n_splits: int = 0, dev_status=None,
+                        stream=None, variant: str = "") -> int:
+    """A whole verify call over the quantised cache (encoding append inside the attention launch, then the
+    combine); returns the split count."""
+    used = ctypes.c_int(0)
+    st = lib(variant).verify_attn_q8_step(_ptr(q), _ptr(k_new), _ptr(v_new), int(q.shape[0]), int(n_live),
+                                          _ptr(k_codes), _ptr(v_codes), _ptr(k_scale), _ptr(v_scale),
+                                          int(k_codes.shape[0]), int(window), _ptr(pos), _ptr(sink), float(scale),
+                                          int(n_splits), _ptr(workspace), _ptr(out), _ptr(out_lse),
+                                          ctypes.byref(used), _ptr(dev_status), _stream(stream))
+    _check("verify_attn_q8_step", st)
     return used.value
 
 

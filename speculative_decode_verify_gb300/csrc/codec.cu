@@ -48,6 +48,12 @@ __global__ void __launch_bounds__(64) append_q8_kernel(const uint2* __restrict__
         return;
     }
     const size_t slot = (size_t)(p % slots);
+    // rows land as if written in row order where the next row writes the same slot (verify rows share
+    // a slot only when they share a position, and then they are adjacent): the earlier row is skipped
+    if (r + 1 < (int)gridDim.x) {
+        const int pn = __ldcg(pos + r + 1);
+        if (pn >= 0 && (size_t)(pn % slots) == slot) return;
+    }
     float x[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u), __uint_as_float(raw.y << 16),
                   __uint_as_float(raw.y & 0xFFFF0000u)};
     if (warp == 0) {
@@ -138,6 +144,40 @@ va_status verify_attn_q8(const va_bf16* q, int n_rows, int n_live, const uint8_t
     a.scale = scale; a.n_rows = n_rows; a.n_live = n_live; a.slots = slots; a.window = window;
     a.n_splits = n_splits; a.n_groups = 1;
     const cudaError_t e = va::launch_attn_q8(a, k_scale, v_scale, (cudaStream_t)stream);
+    if (e != cudaSuccess) return VA_CUDA_ERROR;
+    if (splits_used) *splits_used = n_splits;
+    return VA_OK;
+}
+
+va_status verify_attn_q8_step(const va_bf16* q, const va_bf16* k_new, const va_bf16* v_new, int n_rows, int n_live,
+                              uint8_t* k_codes, int8_t* v_codes, float* k_scale, float* v_scale, int slots, int window,
+                              const int32_t* pos, const float* sink, float scale, int n_splits, float* workspace,
+                              va_bf16* out, float* out_lse, int* splits_used, int32_t* dev_status, va_stream stream) {
+    using va::codec::aligned16;
+    if (!out || !aligned16(out) || !workspace || !aligned16(workspace)) return VA_INVALID_ARG;
+    if (n_live > 0 && (!k_new || !v_new || !aligned16(k_new) || !aligned16(v_new))) return VA_INVALID_ARG;
+    if (!q || !k_codes || !v_codes || !k_scale || !v_scale || !pos) return VA_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_codes) || !aligned16(v_codes) || !aligned16(k_scale) || !aligned16(v_scale))
+        return VA_INVALID_ARG;
+    if (n_rows < 1 || n_rows > VA_MAX_ROWS || n_live < 0 || n_live > n_rows || slots < 1) return VA_INVALID_ARG;
+    if (!std::isfinite(scale) || window < 0 || n_splits < 0 || n_splits > VA_MAX_SPLITS) return VA_INVALID_ARG;
+    if (slots % VA_TILE != 0) return VA_UNSUPPORTED;
+    if (window > 0 && (long long)slots < (long long)window + (n_live > 0 ? n_live - 1 : 0)) return VA_RING_TOO_SMALL;
+    if (n_splits == 0) n_splits = va_auto_splits(window > 0 ? window + (n_live > 0 ? n_live - 1 : 0) : slots, window);
+    float* part_o = workspace;
+    float* part_lse = workspace + (size_t)n_splits * VA_MAX_ROWS * VA_Q_HEADS * VA_HEAD_DIM;
+    va_status st = kv_ring_append_q8(k_new, v_new, n_live, k_codes, v_codes, k_scale, v_scale, slots, pos, dev_status,
+                                     stream);
+    if (st != VA_OK) return st;
+    va::AttnArgs a;
+    a.q = q; a.k = reinterpret_cast<const uint16_t*>(k_codes); a.v = reinterpret_cast<const uint16_t*>(v_codes);
+    a.pos = pos; a.tree = nullptr;
+    a.part_o = part_o; a.part_lse = part_lse; a.dev_status = dev_status;
+    a.scale = scale; a.n_rows = n_rows; a.n_live = n_live; a.slots = slots; a.window = window;
+    a.n_splits = n_splits; a.n_groups = 1;
+    cudaError_t e = va::launch_attn_q8(a, k_scale, v_scale, (cudaStream_t)stream);
+    if (e == cudaSuccess)
+        e = va::launch_combine(part_o, part_lse, n_splits, sink, n_rows, n_live, out, out_lse, (cudaStream_t)stream);
     if (e != cudaSuccess) return VA_CUDA_ERROR;
     if (splits_used) *splits_used = n_splits;
     return VA_OK;

@@ -2,7 +2,10 @@
 
 Bars (one KV head, 48 matrix rows, bf16 output):
   * output: max |out - ref| <= 1e-2 and relative RMS ||out - ref|| / ||ref|| <= 2e-3 over the
-    live rows, where ref is the FP64 oracle rounded once to bf16 (round to nearest even);
+    live rows, where ref is the FP64 oracle rounded once to bf16 (round to nearest even).  Where one
+    bf16 step at |ref| is wider than 1e-2 (|ref| >= 2), an element may differ from ref by that one
+    step: the kernel's fp32 result and the exact one can lie on the two sides of a rounding midpoint,
+    and the output format cannot hold a closer value;
   * per-split LSE: |lse_s - ref| <= 1e-3 over non-empty splits (both -inf counts as equal);
   * padding rows: exactly zero output, LSE -inf.
 """
@@ -13,19 +16,28 @@ OUT_REL_RMS = 2e-3
 LSE_ABS = 1e-3
 
 
+def bf16_step(x):
+    """Spacing of bf16 values at |x| (2^(e - 7) for |x| in [2^e, 2^(e+1)); the subnormal spacing below)."""
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return np.exp2(e - 7)
+
+
 def out_metrics(out, ref, n_live):
-    """out, ref: float arrays [n_rows, 6, 128]; metrics over live rows."""
+    """out, ref: float arrays [n_rows, 6, 128]; metrics over live rows.  over_bar: the largest amount by
+    which an element exceeds its bar max(1e-2, one bf16 step at |ref|) (<= 0 when every element passes)."""
     o = np.asarray(out, dtype=np.float64)[:n_live]
     r = np.asarray(ref, dtype=np.float64)[:n_live]
     diff = o - r
     max_abs = float(np.max(np.abs(diff))) if diff.size else 0.0
+    over = float(np.max(np.abs(diff) - np.maximum(OUT_MAX_ABS, bf16_step(r)))) if diff.size else 0.0
     denom = float(np.linalg.norm(r))
     rel_rms = float(np.linalg.norm(diff) / denom) if denom > 0 else float(np.linalg.norm(diff))
-    return dict(max_abs=max_abs, rel_rms=rel_rms, nan=bool(np.isnan(o).any()))
+    return dict(max_abs=max_abs, over_bar=over, rel_rms=rel_rms, nan=bool(np.isnan(o).any()))
 
 
 def out_ok(m):
-    return (not m["nan"]) and m["max_abs"] <= OUT_MAX_ABS and m["rel_rms"] <= OUT_REL_RMS
+    return (not m["nan"]) and m["over_bar"] <= 0.0 and m["rel_rms"] <= OUT_REL_RMS
 
 
 def lse_err(lse, ref):

@@ -296,3 +296,27 @@ def test_bounded_wait_selftest_argument_checks(L):
     assert L.va_selftest_bounded_wait(0, 0, None, None, None) == va.VA_INVALID_ARG
     assert L.va_selftest_bounded_wait(1_000_000_001, 0, None, None, None) == va.VA_INVALID_ARG
     assert L.va_selftest_bounded_wait(1_000_000, 1_000_001, None, None, None) == va.VA_INVALID_ARG
+
+
+def _q8_step(L, **kw):
+    a = dict(q=FAKE, kn=FAKE, vn=FAKE, n_rows=8, n_live=8, kc=FAKE, vc=FAKE, ks=FAKE, vs=FAKE, slots=4160, W=4096,
+             pos=FAKE, sink=None, scale=0.088, S=4, ws=FAKE, out=FAKE)
+    a.update(kw)
+    return L.verify_attn_q8_step(a["q"], a["kn"], a["vn"], a["n_rows"], a["n_live"], a["kc"], a["vc"], a["ks"],
+                                 a["vs"], a["slots"], a["W"], a["pos"], a["sink"], a["scale"], a["S"], a["ws"],
+                                 a["out"], None, None, None, None)
+
+
+@pytest.mark.parametrize("kw", [dict(out=None), dict(ws=None), dict(ws=ctypes.c_void_p(0x1004)), dict(kn=None),
+                                dict(vn=ctypes.c_void_p(0x1008)), dict(q=None), dict(kc=None), dict(vs=None),
+                                dict(pos=None), dict(ks=ctypes.c_void_p(0x1004)), dict(n_rows=0), dict(n_rows=9),
+                                dict(n_live=9), dict(n_live=-1), dict(slots=0), dict(W=-1), dict(S=-1),
+                                dict(S=4097), dict(scale=float("nan"))])
+def test_q8_step_rejects_bad_arguments(L, kw):
+    assert _q8_step(L, **kw) == va.VA_INVALID_ARG
+
+
+def test_q8_step_ring_checks(L):
+    assert _q8_step(L, slots=4100) == va.VA_UNSUPPORTED
+    assert _q8_step(L, slots=4100, W=0) == va.VA_UNSUPPORTED
+    assert _q8_step(L, slots=4096) == va.VA_RING_TOO_SMALL

@@ -326,3 +326,17 @@ def test_bars_accept_the_oracle_itself():
     res = _run(w)
     m = parity.out_metrics(_bf16_ref(res["out"]), _bf16_ref(res["out"]), w.n_live)
     assert parity.out_ok(m) and m["max_abs"] == 0.0
+
+
+def test_parity_bar_allows_one_bf16_step_only_where_the_step_exceeds_the_bar():
+    import parity
+    assert parity.bf16_step(1.5) == 2.0 ** -7 and parity.bf16_step(3.0) == 2.0 ** -6 and parity.bf16_step(-5.0) == 2.0 ** -5
+    ref = np.full((8, 6, 128), 0.5)
+    out = ref.copy()
+    ref[0, 0, 0], out[0, 0, 0] = 3.0, 3.0 + 2.0 ** -6          # one step at |ref| in [2, 4): allowed
+    assert parity.out_ok(parity.out_metrics(out, ref, 8))
+    out[0, 0, 0] = 3.0 + 2.0 ** -5                             # two steps: not
+    assert not parity.out_ok(parity.out_metrics(out, ref, 8))
+    out[0, 0, 0] = 3.0
+    ref[1, 0, 0], out[1, 0, 0] = 1.5, 1.5 + 0.011              # below 2 the bar stays 1e-2
+    assert not parity.out_ok(parity.out_metrics(out, ref, 8))

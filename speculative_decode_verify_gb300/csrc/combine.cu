@@ -10,15 +10,29 @@
 
 namespace va {
 
-constexpr int kCombineThreads = 256;
-constexpr int kQuarters = 4;                       // column quarters of a matrix row: 32 columns each
-constexpr int kChunks = kD / kQuarters / 4;        // float4 chunks per quarter: 8
+// Shape (measured inside the 192K verify call on GB300, us per call): 512 threads, 4 column parts, 5 splits
+// per thread 25.16; 256 / 4 / 8 25.43; 512 / 2 / 5 25.42; 128 / 4 / 10 26.2; 256 / 8 / 3 26.8; 1024 / 4 / 2
+// 27.9.  Fewer, wider CTAs keep the dependent chain (loads, warp merges, one block barrier) short.
+#ifndef VA_CMB_THREADS
+#define VA_CMB_THREADS 512
+#endif
+#ifndef VA_CMB_PARTS
+#define VA_CMB_PARTS 4
+#endif
+#ifndef VA_CMB_BATCH
+#define VA_CMB_BATCH 5
+#endif
+constexpr int kCombineThreads = VA_CMB_THREADS;
+constexpr int kQuarters = VA_CMB_PARTS;            // column parts of a matrix row (4: 32 columns each)
+constexpr int kChunks = kD / kQuarters / 4;        // float4 chunks per part: 8
 constexpr int kGroups = kCombineThreads / kChunks; // split groups: 32
-constexpr int kBatch = 8;                          // splits per thread loaded together
+constexpr int kBatch = VA_CMB_BATCH;               // splits per thread loaded together
+static_assert(kChunks >= 1 && kChunks <= 32 && (kChunks & (kChunks - 1)) == 0 && kCombineThreads % 32 == 0 &&
+              kD / kQuarters <= kCombineThreads, "combine shape");
 constexpr float kLog2e = 1.4426950408889634f;
 
 // One CTA per (matrix row m = 6 r + h, column quarter).  Thread t owns float4 chunk t % 8 of the quarter
-// and the splits s = t / 8 + 32 i: it issues all of its partial and LSE loads before using any of them.
+// and the splits s = t / 8 + kGroups i: it issues all of its partial and LSE loads before using any of them.
 // Each warp merges its own splits against its own maximum (a two-level log-sum-exp merge), so the CTA
 // needs one barrier: the warp totals are then rescaled to the CTA maximum (which includes the sink) and
 // added in a fixed order: out = sum_s e^(lse_s - M) o_s / (sum_s e^(lse_s - M) + e^(sink - M)).  The
@@ -85,9 +99,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* _
             mx = bm;
         }
     }
-    // within the warp: lanes with the same chunk (lane % 8) hold different splits -> add them
+    // within the warp: lanes with the same chunk (lane % kChunks) hold different splits -> add them
 #pragma unroll
-    for (int off = 8; off < 32; off <<= 1) {
+    for (int off = kChunks; off < 32; off <<= 1) {
         acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
         acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
         acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);

@@ -9,10 +9,11 @@
 // Top-k on GB300 (one launch; the last CTA of each row to finish its tile does the merge):
 //   collect  one CTA per (8,192-logit tile, row): 256 threads x 32 logits from 128-bit loads.  Every
 //            logit gets a 64-bit key (order-preserving value bits, then the complemented token id),
-//            so keys are distinct and "larger key" is exactly the candidate order.  The k-th largest
-//            of the 256 per-thread maxima (warp bitonic sorts, then ranks by binary search) bounds the
-//            tile's k-th key from below, so only logits at or above it - at most k threads' worth - are
-//            ranked.
+//            so keys are distinct and "larger key" is exactly the candidate order.  A lower bound of the
+//            tile's k-th key comes from the per-thread maxima: in every warp, the j-th largest value by
+//            j warp-wide max reductions (j = ceil(k / warps)), then the minimum over the warps (a tile
+//            with fewer than 32 threads of logits takes the exact k-th largest thread maximum, by warp
+//            bitonic sorts and binary searches); only logits at or above it are ranked.
 //   merge    the row's last CTA: the k-th largest of every tile's first few keys bounds the row's k-th
 //            key from below; tiles whose maximum is under it are skipped, the rest contribute the
 //            prefix of their sorted candidates.  The k winners are ranked by counting; one warp then forms the float32
@@ -126,6 +127,7 @@ struct TopkSmem {
     uint64_t all[kMaxMerge];    // merge: every tile's sorted keys
     uint64_t lists[kThreads];   // per-warp sorted thread maxima
     uint64_t red[kThreads / 32];
+    uint32_t wmin[kThreads / 32];
     uint64_t top[kMaxK];
     uint64_t tau;
     float w[kMaxK], run[kMaxK];
@@ -161,7 +163,7 @@ __global__ void __launch_bounds__(kThreads) topk_sample_kernel(const float* __re
                                                                int32_t* __restrict__ tokens, uint64_t* __restrict__ ws,
                                                                unsigned* __restrict__ arrivals) {
     __shared__ TopkSmem sm;
-    const int tile = blockIdx.x, row = blockIdx.y, tid = threadIdx.x, lane = tid & 31;
+    const int tile = blockIdx.x, row = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n_tiles = gridDim.x;
     ptx::griddep_launch_dependents();
     ptx::griddep_wait();
@@ -192,10 +194,32 @@ __global__ void __launch_bounds__(kThreads) topk_sample_kernel(const float* __re
         for (int i = 0; i < w; ++i) mx[i] = mx[i] > mx[i + w] ? mx[i] : mx[i + w];
     const uint64_t tmax = mx[0];
     if (tid == 0) sm.n_cand = 0;
-    // threshold: the k-th largest thread maximum.  The k threads holding the k largest maxima hold at
-    // least k keys at or above it, and a key at or above it can only sit in one of those threads.
-    // (An empty thread offers key 0, below every logit; a tile with fewer than k logits gets 0.)
-    const uint64_t tau = block_kth_largest_u64(tmax, k, sm.lists, &sm.tau);
+    // threshold tau: a lower bound of the tile's k-th largest key, so that every key of the tile's top k is
+    // at or above it.  With f warps whose 32 threads all hold logits, take j = ceil(k / f): in each such
+    // warp, the j-th largest distinct value among its thread maxima (one warp-wide max per round, the
+    // lanes at the maximum dropped), then the minimum over those warps.  Each of the f warps has at least
+    // j threads whose maximum is at or above tau, so at least k distinct keys are: the k-th largest is.
+    // Only the value bits are compared; all keys with the value are kept.  A tile with fewer than 32
+    // threads of logits takes the exact k-th largest thread maximum (an empty thread offers key 0, below
+    // every logit; a tile with fewer than k logits gets 0).
+    uint64_t tau;
+    const int full_warps = min(kThreads, max(0, n4 - base4)) / 32;
+    if (full_warps > 0) {
+        const int j = (k + full_warps - 1) / full_warps;
+        uint32_t v = (uint32_t)(tmax >> 32), m = 0u;
+        for (int r = 0; r < j; ++r) {
+            m = __reduce_max_sync(0xffffffffu, v);
+            v = (v == m) ? 0u : v;
+        }
+        if (lane == 0) sm.wmin[warp] = warp < full_warps ? m : 0xFFFFFFFFu;
+        __syncthreads();
+        uint32_t t = 0xFFFFFFFFu;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) t = min(t, sm.wmin[w]);
+        tau = (uint64_t)t << 32;
+    } else {
+        tau = block_kth_largest_u64(tmax, k, sm.lists, &sm.tau);
+    }
     // compact the keys at or above the threshold: per-thread count, warp scan, one atomic per warp
     unsigned mine = 0;
 #pragma unroll
@@ -245,9 +269,13 @@ __global__ void __launch_bounds__(kThreads) topk_sample_kernel(const float* __re
     }
 
     // ---------------------------------------------------------------- arrival: the last tile merges
-    __threadfence();
+    // (the block barrier orders every thread's key stores before thread 0's fence, which is cumulative:
+    // they are visible before its arrival is)
     __syncthreads();
-    if (tid == 0) sm.last = atomicAdd(arrivals + row, 1u) == (unsigned)(n_tiles - 1);
+    if (tid == 0) {
+        __threadfence();
+        sm.last = atomicAdd(arrivals + row, 1u) == (unsigned)(n_tiles - 1);
+    }
     __syncthreads();
     if (!sm.last) return;
     __threadfence();
@@ -283,20 +311,20 @@ __global__ void __launch_bounds__(kThreads) topk_sample_kernel(const float* __re
     __syncthreads();
     if (tid < 32) {
         // weights, top-p prefix and draw in float32 (IEEE division and expf, in candidate order):
-        // lane j holds candidate j; the running sums are formed in order by lane 0
+        // lane j holds candidate j
         const int n = min(ncm, k);
         const float l0 = ord_to_float((uint32_t)(sm.top[0] >> 32));
         const float w = lane < n
             ? expf(__fdiv_rn(__fsub_rn(ord_to_float((uint32_t)(sm.top[lane] >> 32)), l0), temperature)) : 0.0f;
         sm.w[lane] = w;
-        __syncwarp();
-        if (lane == 0) {
-            float run = 0.0f;
-            for (int j = 0; j < n; ++j) {
-                run = __fadd_rn(run, sm.w[j]);
-                sm.run[j] = run;
-            }
+        // running sums in candidate order: lane j adds w_0, w_1, .. w_j one by one (the same float32 sums
+        // as one sequential pass), all lanes at once
+        float run = 0.0f;
+        for (int j = 0; j < n; ++j) {
+            const float wj = __shfl_sync(0xffffffffu, w, j);
+            if (j <= lane) run = __fadd_rn(run, wj);
         }
+        if (lane < n) sm.run[lane] = run;
         __syncwarp();
         const float total_w = sm.run[n - 1];
         // shortest prefix whose share reaches top_p: the first j with run_j / total >= top_p

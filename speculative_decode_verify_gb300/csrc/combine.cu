@@ -10,25 +10,14 @@
 
 namespace va {
 
-// Shape (measured inside the 192K verify call on GB300, us per call): 512 threads, 4 column parts, 5 splits
-// per thread 25.16; 256 / 4 / 8 25.43; 512 / 2 / 5 25.42; 128 / 4 / 10 26.2; 256 / 8 / 3 26.8; 1024 / 4 / 2
-// 27.9.  Fewer, wider CTAs keep the dependent chain (loads, warp merges, one block barrier) short.
-#ifndef VA_CMB_THREADS
-#define VA_CMB_THREADS 512
-#endif
-#ifndef VA_CMB_PARTS
-#define VA_CMB_PARTS 4
-#endif
-#ifndef VA_CMB_BATCH
-#define VA_CMB_BATCH 5
-#endif
-constexpr int kCombineThreads = VA_CMB_THREADS;
-constexpr int kQuarters = VA_CMB_PARTS;            // column parts of a matrix row (4: 32 columns each)
-constexpr int kChunks = kD / kQuarters / 4;        // float4 chunks per part: 8
-constexpr int kGroups = kCombineThreads / kChunks; // split groups: 32
-constexpr int kBatch = VA_CMB_BATCH;               // splits per thread loaded together
-static_assert(kChunks >= 1 && kChunks <= 32 && (kChunks & (kChunks - 1)) == 0 && kCombineThreads % 32 == 0 &&
-              kD / kQuarters <= kCombineThreads, "combine shape");
+// Block shapes (measured inside the verify call on GB300): up to 8 verify rows (48 matrix rows x 4 column
+// quarters = 192 CTAs), 512 threads with 5 splits per thread: 25.16 us per 192K call, against 25.43 us
+// for 256 x 8, 25.42 for 512 threads over column halves, 26.2-27.9 for 128 / 1024 threads or eighths;
+// fewer, wider CTAs keep the dependent chain (loads, warp merges, one block barrier) short.  A 16-node
+// tree has 96 matrix rows (384 CTAs), which do not all fit at once in 512-thread blocks: there 256
+// threads with 8 splits each.
+constexpr int kQuarters = 4;                       // column quarters of a matrix row: 32 columns each
+constexpr int kChunks = kD / kQuarters / 4;        // float4 chunks per quarter: 8
 constexpr float kLog2e = 1.4426950408889634f;
 
 // One CTA per (matrix row m = 6 r + h, column quarter).  Thread t owns float4 chunk t % 8 of the quarter
@@ -38,13 +27,16 @@ constexpr float kLog2e = 1.4426950408889634f;
 // added in a fixed order: out = sum_s e^(lse_s - M) o_s / (sum_s e^(lse_s - M) + e^(sink - M)).  The
 // exponentials are the hardware exp2 of log2e-scaled differences (the library exp costs a dependent chain
 // of ~30 instructions per weight, which showed as ~1 us of the combine's time).
+template <int kCombineThreads, int kBatch>   // kBatch: splits per thread loaded together
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* __restrict__ part_o,
                                                                   const float* __restrict__ part_lse,
                                                                   int n_splits, const float* __restrict__ sink,
                                                                   int n_rows, int n_live,
                                                                   __nv_bfloat16* __restrict__ out,
                                                                   float* __restrict__ out_lse) {
+    constexpr int kGroups = kCombineThreads / kChunks;   // split groups
     constexpr int kWarps = kCombineThreads / 32;
+    static_assert(kCombineThreads % 32 == 0 && kD / kQuarters <= kCombineThreads, "combine shape");
     __shared__ float4 part[kWarps][kChunks];   // per warp, per chunk: weighted sums (against the warp max)
     __shared__ float zpart[kWarps];            // per warp: sum of weights
     __shared__ float wmax[kWarps];             // per warp: its maximum lse
@@ -145,9 +137,12 @@ cudaError_t launch_combine(const float* part_o, const float* part_lse, int n_spl
                            int n_rows, int n_live, uint16_t* out, float* out_lse, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    pdl_config(&cfg, attr, dim3(n_rows * kH, kQuarters), dim3(kCombineThreads), 0, stream);
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, combine_kernel, part_o, part_lse, n_splits, sink, n_rows, n_live,
-                                             reinterpret_cast<__nv_bfloat16*>(out), out_lse);
+    const bool wide = n_rows <= kMaxRows;
+    pdl_config(&cfg, attr, dim3(n_rows * kH, kQuarters), dim3(wide ? 512 : 256), 0, stream);
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
+    const cudaError_t e =
+        wide ? cudaLaunchKernelEx(&cfg, combine_kernel<512, 5>, part_o, part_lse, n_splits, sink, n_rows, n_live, o, out_lse)
+             : cudaLaunchKernelEx(&cfg, combine_kernel<256, 8>, part_o, part_lse, n_splits, sink, n_rows, n_live, o, out_lse);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -193,6 +193,9 @@ def measured_traffic():
     return None
 
 
+NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, nominal (the measured copy bandwidth is the primary denominator)
+
+
 def measured_peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -216,13 +219,18 @@ def oracle_step_time(w, n_threads: int, min_seconds: float, max_reps: int = 1000
 
 
 def cpu_baseline(w_full):
+    """The oracle on all host cores (the reported value) and on one thread (for scale)."""
     cores = os.cpu_count() or 1
     per_call, reps = oracle_step_time(w_full, cores, 10.0)
+    per_call_1, reps_1 = oracle_step_time(w_full, 1, 4.0, 3)
     hi = int(w_full.pos[w_full.n_live - 1]) + 1
-    return {"value": call_bytes(hi, w_full.n_live) / per_call / 1e9, "unit": "GB/s", "cores": cores,
+    nbytes = call_bytes(hi, w_full.n_live)
+    return {"value": nbytes / per_call / 1e9, "unit": "GB/s", "cores": cores,
             "kind": "oracle",
             "sample": f"{reps} full calls of the 196,608-position, n_live={w_full.n_live} workload "
-                      f"(all 48 row-head pairs, FP64), {cores} threads, {per_call * 1e3:.1f} ms/call"}
+                      f"(all 48 row-head pairs, FP64), {cores} threads, {per_call * 1e3:.1f} ms/call",
+            "single_thread": {"value": nbytes / per_call_1 / 1e9, "unit": "GB/s", "calls": reps_1,
+                              "ms_per_call": per_call_1 * 1e3}}
 
 
 def workload_config():
@@ -920,6 +928,7 @@ def ours(args, dist: Dist):
                    "parallelism": f"replicas x{dist.world} (one KV head per GPU, no collective)"}),
         "us_per_call": t_max / args.steps / len(calls) * 1e6,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "frac_of_nominal": achieved / NOMINAL_HBM_GBS, "nominal_peak": NOMINAL_HBM_GBS,
                      "traffic": measured_traffic(), "kernel": "verify_attn_full split kernel",
                      "us_per_launch": mean_attn * 1e6, "launches": kr * len(calls),
                      "timing": "CUDA events around back-to-back launches over the 5 rotating caches",

@@ -19,6 +19,12 @@ def test_reference_arm_prints_one_json_line_with_the_contract_keys():
         assert key in d, key
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["higher_is_better"] is True
     assert d["steps"] == 2 and d["warmup"] == 1 and d["value"] > 0
+    # value and ms_per_step describe the same timed steps: bytes per step / time per step
+    sys.path.insert(0, ROOT)
+    import bench
+    per_step_bytes = d["value"] * 1e9 * d["ms_per_step"] / 1e3
+    assert abs(per_step_bytes - bench.call_bytes(4096, 8)) / bench.call_bytes(4096, 8) < 0.01
+    assert d["ms_per_step"] > 0.1   # an FP64 CPU verify call over 4,096 positions is not sub-microsecond
     sys.path.insert(0, ROOT)
     import bench
     for k, v in bench.workload_config().items():      # the GPU arm's workload

@@ -182,6 +182,12 @@ __device__ unsigned long long* g_trace = nullptr;
 #define VA_TRACE_TILE(j, k) do { } while (0)
 #endif
 
+#ifdef VA_DEBUG_VISIT
+// Visit map of the debug build: [n_rows][slots] counts, one per (live row, key) let into the softmax,
+// for an exact comparison with the visible-slot sets of the positions.
+__device__ unsigned* g_visit = nullptr;
+#endif
+
 // kAppend: the verify_attn_step instantiation, which writes the live rows itself (a.k_new / a.v_new);
 // the instantiation without it carries none of that code.
 template <bool kAppend>
@@ -637,6 +643,17 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
                 }
 #pragma unroll
                 for (int i = 0; i < kCols; ++i) vis[i] = rv[i / kH];
+#ifdef VA_DEBUG_VISIT
+                if (g_visit) {
+                    int s0, s1, halves;
+                    tile_slots(j, s0, s1, halves);
+                    const int slot = ((L >> 6) ? s1 : s0) + (L & 63);
+                    for (int k = 0; k < kMaxRows / 2; ++k) {
+                        const int r = (kMaxRows / 2) * ch + k;
+                        if (rv[k] && r < n_live_g) atomicAdd(g_visit + (size_t)(kMaxRows * group + r) * a.slots + slot, 1u);
+                    }
+                }
+#endif
             }
             if (j == 0) {
                 // Initial reference of each row: the scaled score of the split's first key when that key
@@ -856,6 +873,15 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace va
+
+#ifdef VA_DEBUG_VISIT
+// Debug build only: point the split kernel's visit map at a device buffer of n_rows x slots unsigned
+// counts, zeroed by the caller (NULL turns it off).
+extern "C" VA_API int va_debug_set_visit(void* device_buffer) {
+    unsigned* p = static_cast<unsigned*>(device_buffer);
+    return cudaMemcpyToSymbol(va::tc::g_visit, &p, sizeof p) == cudaSuccess ? VA_OK : VA_CUDA_ERROR;
+}
+#endif
 
 #ifdef VA_TRACE
 // Debug build only: point the split kernel's timeline probe at a device buffer of n_splits x 256

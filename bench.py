@@ -443,6 +443,59 @@ def ours(args, dist: Dist):
                            "us_per_call": us, "gbs": nbytes / us / 1e3, "frac_of_hbm_peak": nbytes / us / 1e3 / hbm})
         return points
 
+    def tree_short_measure(ctx_short=2048, reps=100, per_graph=8):
+        """A 16-node best-first tree at a short context (nodes at ctx_short - 16 .. ctx_short - 1): per call
+        (kv_ring_append of the nodes + verify_attn_tree + combine), 2 x per_graph calls in one CUDA graph as
+        consecutive layers would run, two caches alternating.  Latency-bound; context for the pages'
+        single-GPU verify figure, which is quoted at a short median context on other hardware."""
+        cap = ctx_short + 64
+        ts = []
+        for i in range(2):
+            w = synth.make_tree(f"bench_tree_short{i}", 540 + i, base=ctx_short - synth.TREE_NODES, slots=cap)
+            k = torch.full((cap, 128), synth.BF16_NAN, dtype=torch.int16, device=dev)
+            v = torch.full((cap, 128), synth.BF16_NAN, dtype=torch.int16, device=dev)
+            k[:w.base] = synth.bits(w.k_hist)[:w.base].to(dev)
+            v[:w.base] = synth.bits(w.v_hist)[:w.base].to(dev)
+            ts.append(dict(w=w, k=k, v=v, q=synth.bits(w.q).to(dev), tree=w.tree.to(dev), pos=w.node_pos.to(dev),
+                           kn=synth.bits(w.k_hist)[w.base:].contiguous().to(dev),
+                           vn=synth.bits(w.v_hist)[w.base:].contiguous().to(dev), sink=w.sink.to(dev),
+                           out=torch.empty(16, 6, 128, dtype=torch.int16, device=dev)))
+        St = va.va_auto_splits_for(cap, 0, torch.cuda.get_device_properties(dev).multi_processor_count // 2)
+        po = torch.empty(St, 16, 6, 128, dtype=torch.float32, device=dev)
+        pl = torch.empty(St, 16, 6, dtype=torch.float32, device=dev)
+
+        def one(c):
+            w = c["w"]
+            st = L.kv_ring_append(P(c["kn"].data_ptr()), P(c["vn"].data_ptr()), w.n_nodes, P(c["k"].data_ptr()),
+                                  P(c["v"].data_ptr()), cap, P(c["pos"].data_ptr()), None, sp)
+            st |= L.verify_attn_tree(P(c["q"].data_ptr()), 16, w.n_nodes, P(c["k"].data_ptr()), P(c["v"].data_ptr()),
+                                     cap, 0, P(c["tree"].data_ptr()), ctypes.c_float(w.scale), St, P(po.data_ptr()),
+                                     P(pl.data_ptr()), None, None, sp)
+            st |= L.attn_split_combine(P(po.data_ptr()), P(pl.data_ptr()), St, P(c["sink"].data_ptr()), 16, w.n_nodes,
+                                       P(c["out"].data_ptr()), None, sp)
+            if st:
+                raise RuntimeError(f"short tree call failed with status {st}")
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                for c in ts:
+                    one(c)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(per_graph):
+                    for c in ts:
+                        one(c)
+            g.replay()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+            e1.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (reps * len(ts) * per_graph)
+        return {"workload": f"16-node best-first draft tree, nodes at {ctx_short - 16:,}..{ctx_short - 1:,} of a "
+                            f"{ctx_short:,}-position full-attention cache", "n_splits": St, "us_per_call": us}
+
     def tree_measure(reps=300):
         """A 16-node best-first draft tree at the 192K extent (nodes at 196,592..196,607): per call
         kv_ring_append of the 16 nodes + verify_attn_tree + attn_split_combine, graph-replayed over three
@@ -509,7 +562,7 @@ def ours(args, dist: Dist):
         return {"workload": "16-node best-first draft tree, nodes at 196,592..196,607 of a 196,608-position "
                             "full-attention cache (100.7 MB K/V), 3 rotating caches",
                 "n_splits": St, "groups": groups, "us_per_call": us_call, "gbs_call": call_b / us_call / 1e3,
-                "attn_us_per_launch": us_attn, "attn_gbs": attn_b / us_attn / 1e3}
+                "attn_us_per_launch": us_attn, "attn_gbs": attn_b / us_attn / 1e3, "short": tree_short_measure()}
 
     def q8_caches(n_caches):
         """Quantised caches of the 192K workload, encoded on the GPU by kv_ring_append_q8 (one call each)."""

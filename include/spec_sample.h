@@ -46,13 +46,17 @@ extern "C" {
 #define VA_SAMPLE_MAX_K 32        /* largest top_k */
 #define VA_SAMPLE_TILE 8192       /* logits per tile of the top-k scan */
 #define VA_SAMPLE_MAX_VOCAB 262144 /* 32 tiles: the merge ranks at most 32 x 32 candidates */
+#define VA_SAMPLE_MAX_ROWS 64       /* rows of one sampling call */
+#define VA_SAMPLE_COUNTER_BYTES 256 /* the workspace's first bytes: one arrival counter per row */
 #define VA_DEV_BAD_PATH 64        /* acceptance inputs that do not describe a valid draft / tree */
 
 /*
  * va_sample_workspace_bytes - device workspace that va_sample_topk_topp needs for n_rows rows of
- * `vocab` logits (per row and 8,192-logit tile: top_k sorted candidates; per row: an arrival
- * counter).  0 for arguments out of range.  Zero-fill a workspace once before its first use
- * (cudaMemsetAsync); every call leaves the counters at zero again.  Calls that may run at the same
+ * `vocab` logits.  Layout: the first VA_SAMPLE_COUNTER_BYTES hold one 32-bit arrival counter per row
+ * (at the same place for every shape), then per row and 8,192-logit tile the top_k sorted candidates
+ * (8 bytes each).  0 for arguments out of range.  Zero-fill a workspace once before its first use
+ * (cudaMemsetAsync); every call leaves the counters at zero again, so one workspace sized for the
+ * largest shape serves calls of any smaller (n_rows, vocab, top_k).  Calls that may run at the same
  * time need separate workspaces.
  */
 VA_API size_t va_sample_workspace_bytes(int n_rows, int vocab, int top_k);
@@ -60,7 +64,7 @@ VA_API size_t va_sample_workspace_bytes(int n_rows, int vocab, int top_k);
 /*
  * va_sample_topk_topp - top-k / temperature / top-p sampling of n_rows rows of logits.
  *   logits        device float [n_rows][vocab] (16-byte aligned; vocab a multiple of 4)
- *   n_rows        1..64
+ *   n_rows        1..VA_SAMPLE_MAX_ROWS (64)
  *   vocab         top_k .. VA_SAMPLE_MAX_VOCAB, a multiple of 4 (160,000 for this model)
  *   top_k         1..VA_SAMPLE_MAX_K (20 for this model)
  *   top_p         (0, 1] (0.95 for this model)

@@ -154,7 +154,7 @@ __device__ uint64_t block_kth_of(const uint64_t* keys, int n, int k, uint64_t* o
 }
 
 // Collection of one tile of one row, then - in the last CTA of the row to finish - the merge and the
-// draw.  ws: [n_rows][n_tiles][k] sorted tile keys (largest first; 0 past the tile's logits), then
+// draw.  ws: [n_rows][n_tiles][k] sorted tile keys (largest first; 0 past the tile's logits); arrivals:
 // [n_rows] arrival counters (zero between calls: the merging CTA resets its row's counter).
 __global__ void __launch_bounds__(kThreads) topk_sample_kernel(const float* __restrict__ logits, int vocab, int k,
                                                                float top_p, float temperature,
@@ -547,11 +547,13 @@ int n_tiles_of(int vocab) { return (vocab + VA_SAMPLE_TILE - 1) / VA_SAMPLE_TILE
 extern "C" {
 
 size_t va_sample_workspace_bytes(int n_rows, int vocab, int top_k) {
-    if (n_rows < 1 || n_rows > 64 || top_k < 1 || top_k > VA_SAMPLE_MAX_K || vocab < top_k ||
+    if (n_rows < 1 || n_rows > VA_SAMPLE_MAX_ROWS || top_k < 1 || top_k > VA_SAMPLE_MAX_K || vocab < top_k ||
         vocab > VA_SAMPLE_MAX_VOCAB)
         return 0;
+    // the arrival counters first, at a place that does not depend on the shape (room for the largest
+    // row count), so that one workspace serves calls of different shapes; then the tile keys
     const size_t keys = sizeof(uint64_t) * (size_t)n_rows * n_tiles_of(vocab) * top_k;
-    return keys + ((sizeof(unsigned) * (size_t)n_rows + 15) & ~(size_t)15);
+    return VA_SAMPLE_COUNTER_BYTES + keys;
 }
 
 va_status va_sample_topk_topp(const float* logits, int n_rows, int vocab, int top_k, float top_p, float temperature,
@@ -563,8 +565,8 @@ va_status va_sample_topk_topp(const float* logits, int n_rows, int vocab, int to
     if (!aligned16(logits) || !aligned16(workspace) || workspace_bytes < need) return VA_INVALID_ARG;
     if (!(top_p > 0.0f && top_p <= 1.0f) || !(temperature > 0.0f) || temperature == INFINITY) return VA_INVALID_ARG;
     const int n_tiles = n_tiles_of(vocab);
-    uint64_t* ws = static_cast<uint64_t*>(workspace);
-    unsigned* arrivals = reinterpret_cast<unsigned*>(ws + (size_t)n_rows * n_tiles * top_k);
+    unsigned* arrivals = static_cast<unsigned*>(workspace);
+    uint64_t* ws = reinterpret_cast<uint64_t*>(static_cast<unsigned char*>(workspace) + VA_SAMPLE_COUNTER_BYTES);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     va::pdl_config(&cfg, attr, dim3(n_tiles, n_rows), dim3(va::smp::kThreads), 0, (cudaStream_t)stream);

@@ -55,6 +55,11 @@ def test_binding_constants_match_header():
         (va.HEAD_DIM, va.Q_HEADS, va.MAX_ROWS, va.TILE, va.MAX_SPLITS)
     assert (d["VA_OK"], d["VA_INVALID_ARG"], d["VA_UNSUPPORTED"], d["VA_RING_TOO_SMALL"], d["VA_CUDA_ERROR"]) == \
         (va.VA_OK, va.VA_INVALID_ARG, va.VA_UNSUPPORTED, va.VA_RING_TOO_SMALL, va.VA_CUDA_ERROR)
+    # the binding's copies of the other limits must not drift from the headers
+    assert d["VA_NOALLOC_MAX_SPLITS"] == va.NOALLOC_MAX_SPLITS
+    assert d["VA_MAX_TREE_NODES"] == va.MAX_TREE_NODES
+    assert (d["VA_SAMPLE_MAX_K"], d["VA_SAMPLE_TILE"], d["VA_SAMPLE_MAX_VOCAB"]) == \
+        (va.SAMPLE_MAX_K, va.SAMPLE_TILE, va.SAMPLE_MAX_VOCAB)
 
 
 def test_page_constants_golden():
@@ -176,7 +181,10 @@ def test_auto_split_policy(L):
 
 # ----------------------------------------------------------------------------- sampling, acceptance, settlement
 def test_sample_workspace_and_argument_checks(L):
-    assert va.va_sample_workspace_bytes(8, 160000, 20) == 8 * 20 * 20 * 8 + 32   # 20 tiles x 20 keys x 8 B + counters
+    # the row counters first (256 B, the same place for every shape), then 20 tiles x 20 keys x 8 B per row
+    assert va.va_sample_workspace_bytes(8, 160000, 20) == 256 + 8 * 20 * 20 * 8
+    assert va.va_sample_workspace_bytes(64, 160000, 20) == 256 + 64 * 20 * 20 * 8
+    assert va.va_sample_workspace_bytes(65, 160000, 20) == 0
     assert va.va_sample_workspace_bytes(0, 160000, 20) == 0
     assert va.va_sample_workspace_bytes(8, 160000, 33) == 0
     assert va.va_sample_workspace_bytes(8, 262148, 20) == 0

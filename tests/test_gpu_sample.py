@@ -226,5 +226,25 @@ def test_sample_workspace_reuse_across_calls():
         torch.cuda.synchronize()
         check_rows(x, ids.cpu().numpy(), probs.cpu().numpy(), counts.cpu().numpy(), tokens.cpu().numpy(), u,
                    20, 0.95, 1.0)
-    tail = ws[-32:].cpu().numpy().view(np.uint32)
-    assert np.all(tail == 0)
+    counters = ws[:256].cpu().numpy().view(np.uint32)
+    assert np.all(counters == 0)
+
+
+def test_sample_workspace_reuse_across_shapes():
+    # one workspace sized for the largest shape serves smaller ones: the row counters sit at the start
+    # whatever the shape, so a smaller call never reads a counter from bytes that held another call's keys
+    big = (16, 160000, 32)
+    ws = torch.zeros(va.va_sample_workspace_bytes(*big), dtype=torch.uint8, device=DEV)
+    shapes = [big, (8, 160000, 20), (3, 40000, 5), (16, 160000, 32), (1, 8192, 1), (8, 160000, 20)]
+    for i, (n, vocab, k) in enumerate(shapes):
+        x = synth.logits(60 + i, n, vocab=vocab)
+        u = synth.uniforms(60 + i, n)
+        ids = torch.empty(n, k, dtype=torch.int32, device=DEV)
+        probs = torch.empty(n, k, dtype=torch.float32, device=DEV)
+        counts = torch.empty(n, dtype=torch.int32, device=DEV)
+        tokens = torch.full((n,), -7, dtype=torch.int32, device=DEV)
+        va.va_sample_topk_topp(x.to(DEV), k, 0.95, 1.0, u.to(DEV), ids, probs, counts, tokens, ws)
+        torch.cuda.synchronize()
+        check_rows(x, ids.cpu().numpy(), probs.cpu().numpy(), counts.cpu().numpy(), tokens.cpu().numpy(), u,
+                   k, 0.95, 1.0)
+        assert np.all(ws[:256].cpu().numpy().view(np.uint32) == 0)

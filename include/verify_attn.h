@@ -216,25 +216,6 @@ VA_API int va_auto_splits_for(int extent_hint, int window, int sm_count);
 VA_API const char *va_status_string(va_status status);
 
 /*
- * verify_attn_full_noalloc - verify_attn_full followed by attn_split_combine, with the split partials
- * kept in a fixed device buffer owned by this library, so that the caller allocates nothing.
- * The pages have no counterpart to this entry point.  It is for callers that cannot allocate device
- * memory when they call this library - a decode loop embedded in another runtime that hands it only
- * tensors and a stream (and no allocator), or a latency-critical loop that must not call cudaMalloc
- * because cudaMalloc can synchronise the device - and therefore cannot provide the part_o / part_lse
- * workspace that verify_attn_full needs.
- *   Scratch: a file-scope device array of VA_NOALLOC_MAX_SPLITS x 8 x 6 x 129 floats (3.96 MB) for the
- *   partials, held in the memory of every GPU that loads this library's device code until the process
- *   exits.  The first call on a device looks up that array's device address (cudaGetSymbolAddress, with
- *   that device current); make that first call before any stream capture.  Every call reuses the same
- *   array and overwrites it completely, so calls that may overlap on the GPU (unordered streams, several
- *   host threads) race with each other: the caller must order them.
- *   Arguments as verify_attn_full (q, n_rows, n_live, k_cache, v_cache, capacity, pos, scale, n_splits,
- *   splits_used, dev_status) and attn_split_combine (sink, out, out_lse).  n_splits 0 means
- *   va_auto_splits(capacity, 0); a count above VA_NOALLOC_MAX_SPLITS returns VA_INVALID_ARG.
- *   Allocates and frees nothing.  Returns VA_OK, VA_INVALID_ARG or VA_CUDA_ERROR.
- */
-/*
  * verify_attn_step - one whole verify call: the append of the live rows, the split attention of a
  * full-attention or sliding-window layer and the combine with the sink, in two launches instead of the
  * three of kv_ring_append + verify_attn_full / verify_attn_swa + attn_split_combine (the append runs
@@ -266,6 +247,26 @@ VA_API va_status verify_attn_step(const va_bf16 *q, const va_bf16 *k_new, const 
                                   int n_splits, float *workspace, va_bf16 *out, float *out_lse,
                                   int *splits_used, int32_t *dev_status, va_stream stream);
 
+/*
+ * verify_attn_full_noalloc - verify_attn_full followed by attn_split_combine, with the split partials
+ * kept in a fixed device buffer owned by this library, so that the caller allocates nothing.
+ * The pages have no counterpart to this entry point.  It is for callers that cannot allocate device
+ * memory when they call this library - a decode loop embedded in another runtime that hands it only
+ * tensors and a stream (and no allocator), or a latency-critical loop that must not call cudaMalloc
+ * because cudaMalloc can synchronise the device - and therefore cannot provide the part_o / part_lse
+ * workspace that verify_attn_full needs.
+ *   Scratch: a file-scope device array of VA_NOALLOC_MAX_SPLITS x 8 x 6 x 129 floats (3.96 MB) for the
+ *   partials, held in the memory of every GPU that loads this library's device code until the process
+ *   exits.  The first call on a device looks up that array's device address (cudaGetSymbolAddress, with
+ *   that device current); make that first call before any stream capture.  Every call reuses the same
+ *   array and overwrites it completely, so calls that may overlap on the GPU (unordered streams, several
+ *   host threads) race with each other: the caller must order them.
+ *   Arguments as verify_attn_full (q, n_rows, n_live, k_cache, v_cache, capacity, pos, scale, n_splits,
+ *   splits_used, dev_status) and attn_split_combine (sink, out, out_lse).  n_splits 0 means
+ *   va_auto_splits(capacity, 0) capped at VA_NOALLOC_MAX_SPLITS; an explicit count above
+ *   VA_NOALLOC_MAX_SPLITS returns VA_INVALID_ARG.
+ *   Allocates and frees nothing.  Returns VA_OK, VA_INVALID_ARG or VA_CUDA_ERROR.
+ */
 #define VA_NOALLOC_MAX_SPLITS 160
 VA_API va_status verify_attn_full_noalloc(const va_bf16 *q, int n_rows, int n_live,
                                           const va_bf16 *k_cache, const va_bf16 *v_cache, int capacity,

@@ -54,7 +54,10 @@ extern "C" VA_API va_status verify_attn_full_noalloc(const va_bf16* q, int n_row
     if (n_rows < 1 || n_rows > VA_MAX_ROWS || n_live < 0 || n_live > n_rows || capacity < 1) return VA_INVALID_ARG;
     if (!(scale == scale) || scale == INFINITY || scale == -INFINITY) return VA_INVALID_ARG;
     if (n_splits < 0) return VA_INVALID_ARG;
-    if (n_splits == 0) n_splits = va_auto_splits(capacity, 0);
+    // auto: the library's split choice, capped at what the fixed scratch holds (a GPU with more SMs than
+    // VA_NOALLOC_MAX_SPLITS then runs fewer, longer splits instead of failing)
+    if (n_splits == 0) n_splits = va_auto_splits(capacity, 0) < VA_NOALLOC_MAX_SPLITS ? va_auto_splits(capacity, 0)
+                                                                                     : VA_NOALLOC_MAX_SPLITS;
     if (n_splits < 1 || n_splits > VA_NOALLOC_MAX_SPLITS) return VA_INVALID_ARG;   // beyond the fixed scratch
 
     float* scratch = nullptr;

@@ -77,7 +77,45 @@ def test_noalloc_matches_allocating_entry_points_on_consecutive_calls():
         assert int(status.item()) == 0
         got = oracle.bf16_bits_to_f64(out.cpu().numpy())
         exp = oracle.bf16_bits_to_f64(ref.cpu().numpy())
-        m = parity.out_metrics(got, exp, w.n_live)
+        m = parity.out_metrics(got, exp, w.n_live, exact=exp)
         assert parity.out_ok(m), m
         assert parity.lse_err(out_lse.cpu().numpy()[:w.n_live], ref_lse.cpu().numpy()[:w.n_live]) <= parity.LSE_ABS
+        assert np.all(out.cpu().numpy()[w.n_live:] == 0)
+        # and against the FP64 oracle directly
+        o = oracle.verify_attn(synth.bits(w.q).numpy(), synth.bits(w.k_hist).numpy(), synth.bits(w.v_hist).numpy(),
+                               w.pos.numpy(), w.n_live, w.sink.numpy(), w.scale, 0, n_splits=S, n_threads=8)
+        m = parity.out_metrics(got, oracle.bf16_bits_to_f64(oracle.f64_to_bf16_bits(o["out"])), w.n_live,
+                               exact=o["out"])
+        assert parity.out_ok(m), m
+        assert parity.lse_err(out_lse.cpu().numpy()[:w.n_live], o["lse"][:w.n_live]) <= parity.LSE_ABS
+
+
+@pytest.mark.gpu
+def test_noalloc_auto_split_count():
+    # n_splits = 0: the library's own choice, capped at the fixed buffer's limit
+    vbuild.build()
+    L = va.lib()
+    dev = torch.device("cuda")
+    P = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())
+    w = synth.make("noalloc_auto", 44, ctx=3000, n_live=5, slots=9000)
+    c = _device_case(w, dev)
+    out = torch.full((w.n_rows, 6, 128), 0x7FC0, dtype=torch.int16, device=dev)
+    out_lse = torch.full((w.n_rows, 6), float("nan"), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    used = ctypes.c_int(0)
+    for _ in range(2):
+        st = L.verify_attn_full_noalloc(P(c["q"]), w.n_rows, w.n_live, P(c["k"]), P(c["v"]), w.slots, P(c["pos"]),
+                                        ctypes.c_float(w.scale), 0, P(c["sink"]), P(out), P(out_lse),
+                                        ctypes.byref(used), P(status),
+                                        ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+        assert st == va.VA_OK
+        assert used.value == min(va.va_auto_splits(w.slots, 0), va.NOALLOC_MAX_SPLITS)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        o = oracle.verify_attn(synth.bits(w.q).numpy(), synth.bits(w.k_hist).numpy(), synth.bits(w.v_hist).numpy(),
+                               w.pos.numpy(), w.n_live, w.sink.numpy(), w.scale, 0, n_splits=used.value, n_threads=8)
+        got = oracle.bf16_bits_to_f64(out.cpu().numpy())
+        m = parity.out_metrics(got, oracle.bf16_bits_to_f64(oracle.f64_to_bf16_bits(o["out"])), w.n_live,
+                               exact=o["out"])
+        assert parity.out_ok(m), m
         assert np.all(out.cpu().numpy()[w.n_live:] == 0)

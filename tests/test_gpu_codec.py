@@ -128,7 +128,7 @@ def expected_q8(w, n_splits):
 
 def _assert(got, ref, w):
     assert got["status"] == 0, hex(got["status"])
-    m = parity.out_metrics(got["out"], ref["out_bf16"], w.n_live)
+    m = parity.out_metrics(got["out"], ref["out_bf16"], w.n_live, exact=ref["out"])
     assert parity.out_ok(m), m
     assert parity.lse_err(got["out_lse"][:w.n_live], ref["lse"][:w.n_live]) <= parity.LSE_ABS
     assert np.all(got["out_bits"][w.n_live:] == 0)

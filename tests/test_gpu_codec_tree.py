@@ -63,7 +63,7 @@ def expected_q8_tree(w: synth.TreeWorkload, n_splits: int):
 def _assert_parity(got, ref, w):
     assert got["status"] == 0, f"device status {got['status']:#x}"
     n = w.n_nodes
-    m = parity.out_metrics(got["out"], ref["out_bf16"], n)
+    m = parity.out_metrics(got["out"], ref["out_bf16"], n, exact=ref["out"])
     assert parity.out_ok(m), m
     assert parity.lse_err(got["out_lse"][:n], ref["lse"][:n]) <= parity.LSE_ABS
     assert np.all(got["out_bits"][n:] == 0) and np.all(np.isneginf(got["out_lse"][n:]))

@@ -24,7 +24,7 @@ def _sms():
 
 def _assert_parity(got, ref, w):
     assert got["status"] == 0, f"device status {got['status']:#x}"
-    m = parity.out_metrics(got["out"], ref["out_bf16"], w.n_live)
+    m = parity.out_metrics(got["out"], ref["out_bf16"], w.n_live, exact=ref["out"])
     assert parity.out_ok(m), m
     assert parity.lse_err(got["out_lse"][:w.n_live], ref["lse"][:w.n_live]) <= parity.LSE_ABS
     assert np.all(got["out_bits"][w.n_live:] == 0)
@@ -79,7 +79,7 @@ def test_step_swa_ring_placement(off):
     got = run_step_fused(w, n_splits=5, wrap_offset=off)
     ref = expected(w, 5)
     assert got["status"] == 0
-    assert parity.out_ok(parity.out_metrics(got["out"], ref["out_bf16"], w.n_live))
+    assert parity.out_ok(parity.out_metrics(got["out"], ref["out_bf16"], w.n_live, exact=ref["out"]))
     _assert_same_as_separate(got, run_step(w, n_splits=5, wrap_offset=off))
 
 

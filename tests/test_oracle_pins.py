@@ -340,3 +340,33 @@ def test_parity_bar_allows_one_bf16_step_only_where_the_step_exceeds_the_bar():
     out[0, 0, 0] = 3.0
     ref[1, 0, 0], out[1, 0, 0] = 1.5, 1.5 + 0.011              # below 2 the bar stays 1e-2
     assert not parity.out_ok(parity.out_metrics(out, ref, 8))
+
+
+def test_unrounded_bar_admits_a_rounding_flip_but_not_a_one_and_a_half_step_error():
+    # against the unrounded result the bar is 1e-2 plus the half step the bf16 output itself costs
+    exact = np.full((8, 6, 128), 0.5)
+    exact[0, 0, 0] = 3.0 + 0.45 * 2.0 ** -6          # |exact| in [2, 4): one bf16 step is 2^-6
+    ref = oracle.bf16_bits_to_f64(oracle.f64_to_bf16_bits(exact))
+    assert ref[0, 0, 0] == 3.0
+    out = ref.copy()
+    out[0, 0, 0] = 3.0 + 2.0 ** -6                    # the neighbouring value: a rounding flip, allowed
+    m = parity.out_metrics(out, ref, 8, exact=exact)
+    assert parity.out_ok(m) and m["max_abs_exact"] < 1e-2 + 0.5 * 2.0 ** -6
+    out[0, 0, 0] = 3.0 + 1.5 * 2.0 ** -6 + 1e-2       # 1.5 steps + 1e-2 beyond the rounded reference: rejected
+    assert not parity.out_ok(parity.out_metrics(out, ref, 8, exact=exact))
+    # in [4, 8) one step is 2^-5: the grid bar admits a step on either side of the rounded reference, the
+    # unrounded bar only the side a rounding flip can reach
+    exact[0, 0, 0] = 5.0 + 0.4 * 2.0 ** -5
+    ref = oracle.bf16_bits_to_f64(oracle.f64_to_bf16_bits(exact))
+    assert ref[0, 0, 0] == 5.0
+    out = ref.copy()
+    out[0, 0, 0] = 5.0 + 2.0 ** -5                    # flip upwards: 0.6 step from exact, allowed
+    assert parity.out_ok(parity.out_metrics(out, ref, 8, exact=exact))
+    out[0, 0, 0] = 5.0 - 2.0 ** -5                    # one step down: 1.4 steps (0.044) from exact, rejected
+    m = parity.out_metrics(out, ref, 8, exact=exact)
+    assert m["over_bar"] <= 0.0 and not parity.out_ok(m)
+    exact[0, 0, 0] = 5.0                              # on the grid: a one-step output is a 0.031 error
+    ref = oracle.bf16_bits_to_f64(oracle.f64_to_bf16_bits(exact))
+    out = ref.copy()
+    out[0, 0, 0] = 5.0 + 2.0 ** -5
+    assert not parity.out_ok(parity.out_metrics(out, ref, 8, exact=exact))

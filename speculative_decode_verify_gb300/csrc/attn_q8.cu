@@ -791,8 +791,10 @@ bool encode_codes_map(CUtensorMap* map, const void* base, int rows, int box_rows
 cudaError_t launch_attn_q8(const AttnArgs& a, const float* k_scale, const float* v_scale, cudaStream_t stream) {
     if (a.n_groups < 1 || a.n_groups * kMaxRows < a.n_rows || (a.n_groups > 1 && !a.tree)) return cudaErrorInvalidValue;
     CUtensorMap tmq, tmk, tmv, tmk2, tmv2;
-    if (!tc::encode_rows_map(&tmq, a.q, a.n_rows * kH, kMaxM) || !q8::encode_codes_map(&tmk, a.k, a.slots, 64) || !q8::encode_codes_map(&tmv, a.v, a.slots, 64) ||
-        !q8::encode_codes_map(&tmk2, a.k, a.slots, 128) || !q8::encode_codes_map(&tmv2, a.v, a.slots, 128))
+    const tc::MapEncodeFn rows = tc::encode_rows_map, codes = q8::encode_codes_map;
+    if (!tc::cached_map(&tmq, rows, a.q, a.n_rows * kH, kMaxM) || !tc::cached_map(&tmk, codes, a.k, a.slots, 64) ||
+        !tc::cached_map(&tmv, codes, a.v, a.slots, 64) || !tc::cached_map(&tmk2, codes, a.k, a.slots, 128) ||
+        !tc::cached_map(&tmv2, codes, a.v, a.slots, 128))
         return cudaErrorInvalidValue;
     cudaError_t e = ensure_smem_attr((const void*)q8::attn_q8_kernel, (int)q8::kSmemBytes);
     if (e != cudaSuccess) return e;

@@ -851,14 +851,43 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int rows, int box_rows)
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Tensor maps already encoded by this host thread.  A map is a function of (address, rows, box, format)
+// alone, so a caller that passes the same cache or q buffer again reuses its encoding instead of paying
+// for cuTensorMapEncodeTiled on every call; a new address is a new key (no invalidation is needed).
+bool cached_map(CUtensorMap* map, MapEncodeFn encode, const void* base, int rows, int box_rows) {
+    struct Key {
+        MapEncodeFn encode;
+        const void* base;
+        int rows, box_rows;
+    };
+    constexpr int kEntries = 32;
+    thread_local Key keys[kEntries];
+    thread_local CUtensorMap maps[kEntries];
+    thread_local int used = 0, next = 0;
+    for (int i = 0; i < used; ++i) {
+        const Key& k = keys[i];
+        if (k.encode == encode && k.base == base && k.rows == rows && k.box_rows == box_rows) {
+            *map = maps[i];
+            return true;
+        }
+    }
+    if (!encode(map, base, rows, box_rows)) return false;
+    const int slot = used < kEntries ? used++ : next;
+    next = (slot + 1) % kEntries;
+    keys[slot] = Key{encode, base, rows, box_rows};
+    maps[slot] = *map;
+    return true;
+}
+
 }  // namespace tc
 
 cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
     if (a.n_groups < 1 || a.n_groups * kMaxRows < a.n_rows || (a.n_groups > 1 && !a.tree)) return cudaErrorInvalidValue;
     CUtensorMap tmq, tmk, tmv, tmk2, tmv2;
-    if (!tc::encode_rows_map(&tmq, a.q, a.n_rows * kH, 48) || !tc::encode_rows_map(&tmk, a.k, a.slots, 64) ||
-        !tc::encode_rows_map(&tmv, a.v, a.slots, 64) || !tc::encode_rows_map(&tmk2, a.k, a.slots, 128) ||
-        !tc::encode_rows_map(&tmv2, a.v, a.slots, 128))
+    const tc::MapEncodeFn enc = tc::encode_rows_map;
+    if (!tc::cached_map(&tmq, enc, a.q, a.n_rows * kH, 48) || !tc::cached_map(&tmk, enc, a.k, a.slots, 64) ||
+        !tc::cached_map(&tmv, enc, a.v, a.slots, 64) || !tc::cached_map(&tmk2, enc, a.k, a.slots, 128) ||
+        !tc::cached_map(&tmv2, enc, a.v, a.slots, 128))
         return cudaErrorInvalidValue;
     const bool append = a.k_new != nullptr;
     cudaError_t e = ensure_smem_attr(append ? (const void*)tc::attn_tc_kernel<true> : (const void*)tc::attn_tc_kernel<false>,

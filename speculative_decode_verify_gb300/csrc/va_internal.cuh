@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -116,6 +117,13 @@ __device__ __forceinline__ Plan make_tree_plan(int base, const int (&anc)[kMaxNo
     deal_tiles(P, n_splits, split);
     return P;
 }
+
+// Host-side tensor-map encoders (attn_tc.cu, attn_q8.cu) and the per-thread cache of their results.
+namespace tc {
+typedef bool (*MapEncodeFn)(CUtensorMap* map, const void* base, int rows, int box_rows);
+bool encode_rows_map(CUtensorMap* map, const void* base, int rows, int box_rows);
+bool cached_map(CUtensorMap* map, MapEncodeFn encode, const void* base, int rows, int box_rows);
+}  // namespace tc
 
 // Opt a kernel into `bytes` of dynamic shared memory on the current device, once per device
 // (so that a later launch under stream capture issues no attribute call).

@@ -78,6 +78,17 @@ def parse():
     ap.add_argument("--caches", type=int, default=5, help="distinct 192K caches to rotate (1..5)")
     ap.add_argument("--variant", default="", help="library build variant to load (A/B tuning aid)")
     ap.add_argument("--ctx", type=int, default=CTX, help="context of the --kernel-only runs")
+    ap.add_argument("--ab", nargs=2, metavar=("A", "B"), default=None,
+                    help="A/B comparison of two library builds on one GPU, alternated in ABBA BAAB order: each "
+                         "argument is a comma-separated list of NAME=VALUE compile definitions ('' = the default "
+                         "build); prints one JSON line with each build's per-block times and their spread")
+    ap.add_argument("--ab-what", choices=["call", "kernel"], default="call",
+                    help="A/B unit: a whole verify call (verify_attn_step, graph-replayed) or the split-attention "
+                         "launch alone (verify_attn_full, back to back)")
+    ap.add_argument("--ab-ctx", type=int, default=CTX, help="A/B workload context (positions)")
+    ap.add_argument("--ab-window", type=int, default=0, help="A/B workload window (0 = full attention)")
+    ap.add_argument("--ab-blocks", type=int, default=16, help="A/B timed blocks per build (a multiple of 4)")
+    ap.add_argument("--ab-reps", type=int, default=40, help="graph replays (or launch rounds) per A/B block")
     return ap.parse_args()
 
 
@@ -211,10 +222,11 @@ def oracle_step_time(w, n_threads: int, min_seconds: float, max_reps: int = 1000
     oracle.verify_attn(qb, kb[:64], vb[:64], [0] * w.n_rows, 1, w.sink.numpy(), w.scale, 0, n_threads=1)
     reps, t0 = 0, time.perf_counter()
     while True:
-        oracle.verify_attn(qb, kb, vb, w.pos.numpy(), w.n_live, w.sink.numpy(), w.scale, 0, n_threads=n_threads)
+        res = oracle.verify_attn(qb, kb, vb, w.pos.numpy(), w.n_live, w.sink.numpy(), w.scale, 0, n_threads=n_threads)
         reps += 1
         el = time.perf_counter() - t0
         if el >= min_seconds or reps >= max_reps:
+            oracle_step_time.last = res
             return el / reps, reps
 
 
@@ -233,6 +245,26 @@ def cpu_baseline(w_full):
                               "ms_per_call": per_call_1 * 1e3}}
 
 
+def parity_fields(out_bits, out_lse, ref, n_live: int):
+    """The GPU call's output against the oracle's for the same inputs: max |out - ref| with ref rounded once
+    to bf16, max |out - exact| against the unrounded FP64 result, relative RMS, output LSE error."""
+    import numpy as np
+
+    import oracle
+    exact = np.asarray(ref["out"], dtype=np.float64)[:n_live]
+    got = oracle.bf16_bits_to_f64(np.asarray(out_bits))[:n_live]
+    rounded = oracle.bf16_bits_to_f64(oracle.f64_to_bf16_bits(exact))
+    a = np.abs(got - exact)
+    step = np.exp2(np.floor(np.log2(np.maximum(np.maximum(np.abs(exact), np.abs(got)), 2.0 ** -126))) - 7)
+    return {"call": f"196,608 positions, n_live={n_live}", "max_abs": float(np.abs(got - rounded).max()),
+            "max_abs_exact": float(a.max()), "exact_bar_ok": bool(np.all(a <= 1e-2 + 0.5 * step)),
+            "rel_rms": float(np.linalg.norm(got - rounded) / np.linalg.norm(rounded)),
+            "lse_max_abs": float(np.abs(np.asarray(out_lse, dtype=np.float64)[:n_live] -
+                                        np.asarray(ref["lse"], dtype=np.float64)[:n_live]).max()),
+            "bars": "max_abs <= 1e-2 (one bf16 step where wider), |out - exact| <= 1e-2 + half a step, "
+                    "rel_rms <= 2e-3, lse <= 1e-3"}
+
+
 def workload_config():
     """The workload both arms report (the GPU arm adds how it ran it)."""
     return {"workload": "full-attention verify, 196,608 positions (100.7 MB bf16 K/V), 1 KV head / 6 q heads, d 128, "
@@ -241,30 +273,41 @@ def workload_config():
 
 
 def reference_arm(args, dist: Dist):
+    """The oracle as the reference arm, on the same workload as the GPU arm: per step the five 196,608-position
+    calls (n_live 4..8), each the plain FP64 definition over all 48 row-head pairs on every host core."""
     if dist.rank != 0:
         return
+    import oracle
     from speculative_decode_verify_gb300 import synth
-    # bounded sample per step: the same verify call (8 rows, 48 row-head pairs, FP64) over a
-    # 4,096-position prefix of the synthetic history
-    w = synth.full_192k(8)
-    w.k_hist, w.v_hist = w.k_hist[:4096].clone(), w.v_hist[:4096].clone()
-    w.pos = synth.tail_positions(4096, 8)
     cores = os.cpu_count() or 1
+    calls = []
+    for n in N_LIVES:
+        w = synth.full_192k(n)
+        calls.append((synth.bits(w.q).numpy(), synth.bits(w.k_hist).numpy(), synth.bits(w.v_hist).numpy(),
+                      w.pos.numpy(), n, w.sink.numpy(), w.scale))
+    oracle.verify_attn(calls[0][0], calls[0][1][:64], calls[0][2][:64], [0] * 8, 1, calls[0][5], calls[0][6], 0,
+                       n_threads=1)
+
+    def step():
+        for qb, kb, vb, pos, n, sink, scale in calls:
+            oracle.verify_attn(qb, kb, vb, pos, n, sink, scale, 0, n_threads=cores)
+
     for _ in range(max(args.warmup, 1)):
-        oracle_step_time(w, cores, 0.0, 1)
+        step()
     t0 = time.perf_counter()
-    per, _ = oracle_step_time(w, cores, float("inf"), args.steps)   # exactly args.steps calls
+    for _ in range(args.steps):
+        step()
     total = time.perf_counter() - t0
-    bytes_step = call_bytes(4096, 8)
+    bytes_step = sum(call_bytes(CTX, n) for n in N_LIVES)
     value = bytes_step * args.steps / total / 1e9
-    sample = (f"per step one FP64 oracle call: 8 rows x 6 heads over a 4,096-position prefix of the 196,608-"
-              f"position history, {cores} threads")
+    sample = (f"per step the five verify calls of the GPU arm's workload (196,608 positions, n_live 4..8, 8 rows x 6 "
+              f"heads, FP64 oracle), {cores} threads, {total / args.steps / len(N_LIVES) * 1e3:.1f} ms per call")
     print(json.dumps({"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
                       "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / args.steps * 1e3,
                       "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                       "data": "synthetic",
-                      "config": dict(workload_config(), timing="wall clock on the host cores, a bounded sample "
-                                                                               "per step (cpu_baseline.sample)"),
+                      "config": dict(workload_config(), timing="wall clock on the host cores over the same five "
+                                                               "calls per step as the GPU arm"),
                       "cpu_baseline": {"value": value, "unit": "GB/s", "kind": "oracle", "cores": cores,
                                        "sample": sample},
                       "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}))
@@ -1002,6 +1045,9 @@ def ours(args, dist: Dist):
     }
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w8)
+        c8 = next(c for c in calls if c["n"] == 8)
+        line["parity"] = parity_fields(c8["out"].cpu().numpy().view("uint16"), c8["out_lse"].cpu().numpy(),
+                                       oracle_step_time.last, 8)
     if dist.rank == 0:
         print(json.dumps(line))
 
@@ -1067,12 +1113,143 @@ def profiling_loop(args, L, dev, stream):
                       "gbs": nbytes / us / 1e3}))
 
 
+def ab_order(n_blocks: int):
+    """Drift-cancelling order of two arms ("Qwen3.8-27B on one RTX 4090", "Checking the path that actually
+    runs"): ABBA then BAAB, repeated, so a linear drift in clocks or temperature weighs both arms equally."""
+    pattern = "ABBABAAB"
+    return [pattern[i % len(pattern)] for i in range(2 * n_blocks)]
+
+
+def ab_compare(args, dist: Dist):
+    """Two library builds, the same seeded workload, alternated block by block on one GPU."""
+    import ctypes
+    import hashlib
+
+    import torch
+
+    import speculative_decode_verify_gb300 as va
+    from speculative_decode_verify_gb300 import build as vbuild
+    from speculative_decode_verify_gb300 import synth
+
+    if dist.rank != 0:
+        return
+    arms = {}
+    for tag, spec in zip("AB", args.ab):
+        defs = tuple(d.strip() for d in spec.split(",") if d.strip())
+        name = "_ab" + hashlib.sha1(",".join(defs).encode()).hexdigest()[:10] if defs else ""
+        vbuild.build(variant=name, defines=defs)
+        arms[tag] = dict(spec=spec or "(default build)", lib=va.lib(name), times=[])
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    P = ctypes.c_void_p
+    ctx, window = args.ab_ctx, args.ab_window
+    slots = synth.RING_SLOTS if window else ctx + 64
+    n_caches = 5 if 512 * ctx > (32 << 20) else 2
+    caches = []
+    for i in range(n_caches):
+        w = synth.make(f"ab{ctx}_{window}", 950 + i, ctx=ctx, n_live=8, window=window, slots=slots)
+        kb, vb = synth.bits(w.k_hist), synth.bits(w.v_hist)
+        k = torch.full((slots, 128), synth.BF16_NAN, dtype=torch.int16)
+        v = torch.full((slots, 128), synth.BF16_NAN, dtype=torch.int16)
+        first = max(0, ctx - slots) if window else 0
+        pp = torch.arange(first, ctx)
+        k[pp % slots], v[pp % slots] = kb[first:ctx], vb[first:ctx]
+        caches.append(dict(w=w, kb=kb, vb=vb, k=k.to(dev), v=v.to(dev), q=synth.bits(w.q).to(dev),
+                           sink=w.sink.to(dev)))
+    calls = []
+    for j in range(15):                      # three rounds of n_live 4..8 per graph
+        n, c = N_LIVES[j % len(N_LIVES)], caches[j % n_caches]
+        pos = synth.tail_positions(ctx, n)
+        idx = pos[:n].to(torch.int64)
+        calls.append(dict(c=c, n=n, pos=pos.to(dev), kn=c["kb"][idx].contiguous().to(dev),
+                          vn=c["vb"][idx].contiguous().to(dev),
+                          out=torch.empty(8, 6, 128, dtype=torch.int16, device=dev)))
+    S = va.va_auto_splits(window + 7 if window else slots, window)
+    ws = torch.zeros(va.va_workspace_bytes(S) // 4, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def launch(L, x):
+        c = x["c"]
+        if args.ab_what == "call":
+            st = L.verify_attn_step(P(c["q"].data_ptr()), P(x["kn"].data_ptr()), P(x["vn"].data_ptr()), 8, x["n"],
+                                    P(c["k"].data_ptr()), P(c["v"].data_ptr()), slots, window, P(x["pos"].data_ptr()),
+                                    P(c["sink"].data_ptr()), ctypes.c_float(synth.SCALE), S, P(ws.data_ptr()),
+                                    P(x["out"].data_ptr()), None, None, P(status.data_ptr()), sp)
+        else:
+            po = ws.data_ptr()
+            pl = po + 4 * S * 8 * 6 * 128
+            fn = L.verify_attn_swa if window else L.verify_attn_full
+            extra = (slots, window) if window else (slots,)
+            st = fn(P(c["q"].data_ptr()), 8, x["n"], P(c["k"].data_ptr()), P(c["v"].data_ptr()), *extra,
+                    P(x["pos"].data_ptr()), ctypes.c_float(synth.SCALE), S, P(po), P(pl), None,
+                    P(status.data_ptr()), sp)
+        if st:
+            raise RuntimeError(f"A/B launch failed with status {st}")
+
+    with torch.cuda.stream(stream):
+        graphs = {}
+        for tag, arm in arms.items():
+            for _ in range(3):
+                for x in calls:
+                    launch(arm["lib"], x)
+            if args.ab_what == "call":
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for x in calls:
+                        launch(arm["lib"], x)
+                graphs[tag] = g
+        stream.synchronize()
+        outs = {}
+        for tag, arm in arms.items():   # both builds must compute the same thing
+            if args.ab_what == "call":
+                graphs[tag].replay()
+            else:
+                for x in calls:
+                    launch(arm["lib"], x)
+            stream.synchronize()
+            outs[tag] = torch.stack([x["out"].clone() for x in calls]) if args.ab_what == "call" else \
+                ws.clone()
+        same = bool(torch.equal(outs["A"], outs["B"]))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for tag in ab_order(max(4, args.ab_blocks)):
+            arm = arms[tag]
+            if args.ab_what == "call":
+                graphs[tag].replay()            # untimed: the block starts from a warm graph
+            e0.record(stream)
+            for _ in range(args.ab_reps):
+                if args.ab_what == "call":
+                    graphs[tag].replay()
+                else:
+                    for x in calls:
+                        launch(arm["lib"], x)
+            e1.record(stream)
+            e1.synchronize()
+            arm["times"].append(e0.elapsed_time(e1) * 1e3 / (args.ab_reps * len(calls)))
+    if int(status.item()) != 0:
+        raise RuntimeError(f"A/B run: device status {int(status.item()):#x}")
+    res = {}
+    for tag, arm in arms.items():
+        t = arm["times"]
+        res[tag] = {"defines": arm["spec"], "us_median": statistics.median(t), "us_min": min(t), "us_max": max(t),
+                    "us_stdev": statistics.stdev(t) if len(t) > 1 else 0.0, "blocks": [round(x, 3) for x in t]}
+    d = [b - a for a, b in zip(arms["A"]["times"], arms["B"]["times"])]
+    print(json.dumps({"ab": args.ab_what, "ctx": ctx, "window": window, "n_splits": S, "calls_per_block":
+                      args.ab_reps * len(calls), "order": "ABBA BAAB", "A": res["A"], "B": res["B"],
+                      "b_minus_a_us_median": statistics.median(d), "b_minus_a_us_min": min(d),
+                      "b_minus_a_us_max": max(d), "outputs_identical": same,
+                      "unit": "us per verify call" if args.ab_what == "call" else "us per split-attention launch"}))
+
+
 def main():
     args = parse()
     dist = Dist()
     try:
         if args.impl == "reference":
             reference_arm(args, dist)
+        elif args.ab:
+            ab_compare(args, dist)
         else:
             ours(args, dist)
     finally:

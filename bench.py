@@ -207,6 +207,27 @@ def measured_traffic():
 NOMINAL_HBM_GBS = 7900.0   # GB300 HBM3e, nominal (the measured copy bandwidth is the primary denominator)
 
 
+def cudart():
+    """The CUDA toolkit's runtime library (for plain cudaMemcpyAsync / cudaStreamSynchronize calls)."""
+    import ctypes
+    import glob
+    names = [os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "lib64", "libcudart.so")]
+    names += sorted(glob.glob("/usr/local/cuda*/lib64/libcudart.so*")) + ["libcudart.so"]
+    for n in names:
+        try:
+            rt = ctypes.CDLL(n)
+            break
+        except OSError:
+            continue
+    else:
+        raise RuntimeError("libcudart not found")
+    rt.cudaMemcpyAsync.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p]
+    rt.cudaMemcpyAsync.restype = ctypes.c_int
+    rt.cudaStreamSynchronize.argtypes = [ctypes.c_void_p]
+    rt.cudaStreamSynchronize.restype = ctypes.c_int
+    return rt
+
+
 def measured_peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -392,12 +413,17 @@ def ours(args, dist: Dist):
     sp = ctypes.c_void_p(stream.cuda_stream)
     P = ctypes.c_void_p
 
+    # each call's C-ABI arguments, marshalled once (a caller that repeats a call keeps its pointers)
+    for c in calls:
+        c["step_args"] = (P(c["q"].data_ptr()), P(c["kn"].data_ptr()), P(c["vn"].data_ptr()), 8, c["n"],
+                          P(c["k"].data_ptr()), P(c["v"].data_ptr()), CAPACITY, 0, P(c["pos"].data_ptr()),
+                          P(c["sink"].data_ptr()), ctypes.c_float(c["scale"]), S, P(ws.data_ptr()),
+                          P(c["out"].data_ptr()), P(c["out_lse"].data_ptr()), None, None, sp)
+    step_fn = L.verify_attn_step
+
     def launch_call(c):
         # one verify call through verify_attn_step: the append inside the attention launch, then the combine
-        st = L.verify_attn_step(P(c["q"].data_ptr()), P(c["kn"].data_ptr()), P(c["vn"].data_ptr()), 8, c["n"],
-                                P(c["k"].data_ptr()), P(c["v"].data_ptr()), CAPACITY, 0, P(c["pos"].data_ptr()),
-                                P(c["sink"].data_ptr()), ctypes.c_float(c["scale"]), S, P(ws.data_ptr()),
-                                P(c["out"].data_ptr()), P(c["out_lse"].data_ptr()), None, None, sp)
+        st = step_fn(*c["step_args"])
         if st:
             raise RuntimeError(f"verify_attn_step failed with status {st}")
 
@@ -966,14 +992,21 @@ def ours(args, dist: Dist):
         ke = args.steps
         dist.barrier()
         torch.cuda.synchronize(dev)
+        # the copies through the CUDA runtime's cudaMemcpyAsync (as a C caller of the library would issue
+        # them), the calls through the C ABI, one cudaStreamSynchronize per step
+        rt = cudart()
+        memcpy = rt.cudaMemcpyAsync
+        sync = rt.cudaStreamSynchronize
+        h2d_args = (P(in_d.data_ptr()), P(in_h.data_ptr()), in_bytes, 1, sp)    # cudaMemcpyHostToDevice
+        d2h_args = (P(out_h.data_ptr()), P(out_d.data_ptr()), out_bytes, 2, sp)  # cudaMemcpyDeviceToHost
         t0 = time.perf_counter()
-        with torch.cuda.stream(stream):
-            for _ in range(ke):
-                in_d.copy_(in_h, non_blocking=True)
-                for c in calls:
-                    launch_call(c)
-                out_h.copy_(out_d, non_blocking=True)
-                stream.synchronize()
+        for _ in range(ke):
+            if memcpy(*h2d_args):
+                raise RuntimeError("cudaMemcpyAsync (inputs) failed")
+            for c in calls:
+                launch_call(c)
+            if memcpy(*d2h_args) or sync(sp):
+                raise RuntimeError("cudaMemcpyAsync (outputs) or cudaStreamSynchronize failed")
         t_e2e = time.perf_counter() - t0
         # the same end-to-end step as one CUDA graph (both copies and the five calls), replayed and
         # synchronised once per step: how a serving loop that captures its step would drive the library
@@ -1166,11 +1199,15 @@ def ab_compare(args, dist: Dist):
         calls.append(dict(c=c, n=n, pos=pos.to(dev), kn=c["kb"][idx].contiguous().to(dev),
                           vn=c["vb"][idx].contiguous().to(dev),
                           out=torch.empty(8, 6, 128, dtype=torch.int16, device=dev)))
-    S = va.va_auto_splits(window + 7 if window else slots, window)
+    # each build picks its own split count (the split policy is one of the things an A/B may change)
+    for arm in arms.values():
+        arm["S"] = arm["lib"].va_auto_splits(window + 7 if window else slots, window)
+    S = max(arm["S"] for arm in arms.values())
     ws = torch.zeros(va.va_workspace_bytes(S) // 4, dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
-    def launch(L, x):
+    def launch(arm, x):
+        L, S = arm["lib"], arm["S"]
         c = x["c"]
         if args.ab_what == "call":
             st = L.verify_attn_step(P(c["q"].data_ptr()), P(x["kn"].data_ptr()), P(x["vn"].data_ptr()), 8, x["n"],
@@ -1193,12 +1230,12 @@ def ab_compare(args, dist: Dist):
         for tag, arm in arms.items():
             for _ in range(3):
                 for x in calls:
-                    launch(arm["lib"], x)
+                    launch(arm, x)
             if args.ab_what == "call":
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=stream):
                     for x in calls:
-                        launch(arm["lib"], x)
+                        launch(arm, x)
                 graphs[tag] = g
         stream.synchronize()
         outs = {}
@@ -1207,7 +1244,7 @@ def ab_compare(args, dist: Dist):
                 graphs[tag].replay()
             else:
                 for x in calls:
-                    launch(arm["lib"], x)
+                    launch(arm, x)
             stream.synchronize()
             outs[tag] = torch.stack([x["out"].clone() for x in calls]) if args.ab_what == "call" else \
                 ws.clone()
@@ -1223,7 +1260,7 @@ def ab_compare(args, dist: Dist):
                     graphs[tag].replay()
                 else:
                     for x in calls:
-                        launch(arm["lib"], x)
+                        launch(arm, x)
             e1.record(stream)
             e1.synchronize()
             arm["times"].append(e0.elapsed_time(e1) * 1e3 / (args.ab_reps * len(calls)))
@@ -1235,7 +1272,8 @@ def ab_compare(args, dist: Dist):
         res[tag] = {"defines": arm["spec"], "us_median": statistics.median(t), "us_min": min(t), "us_max": max(t),
                     "us_stdev": statistics.stdev(t) if len(t) > 1 else 0.0, "blocks": [round(x, 3) for x in t]}
     d = [b - a for a, b in zip(arms["A"]["times"], arms["B"]["times"])]
-    print(json.dumps({"ab": args.ab_what, "ctx": ctx, "window": window, "n_splits": S, "calls_per_block":
+    print(json.dumps({"ab": args.ab_what, "ctx": ctx, "window": window, "n_splits": [arms["A"]["S"], arms["B"]["S"]],
+                      "calls_per_block":
                       args.ab_reps * len(calls), "order": "ABBA BAAB", "A": res["A"], "B": res["B"],
                       "b_minus_a_us_median": statistics.median(d), "b_minus_a_us_min": min(d),
                       "b_minus_a_us_max": max(d), "outputs_identical": same,

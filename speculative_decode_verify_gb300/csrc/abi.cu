@@ -6,6 +6,10 @@
 
 #include "va_internal.cuh"
 
+#ifndef VA_MIN_SPLIT_TILES
+#define VA_MIN_SPLIT_TILES 2
+#endif
+
 namespace va {
 
 int device_sm_count();   // also called by codec.cu
@@ -217,12 +221,12 @@ size_t va_workspace_bytes(int n_splits) {
 
 int va_auto_splits_for(int extent_hint, int window, int sm_count) {
     // One split per SM at most (the split kernel holds a whole SM's shared memory); at least
-    // two 64-position tiles per split so that each split amortises its partial write.
+    // VA_MIN_SPLIT_TILES 64-position tiles per split so that each split amortises its partial write.
     if (sm_count < 1) sm_count = 148;
     long long extent = extent_hint > 0 ? extent_hint : 1;
     if (window > 0 && extent > (long long)window + VA_MAX_ROWS - 1) extent = (long long)window + VA_MAX_ROWS - 1;
     const long long tiles = (extent + VA_TILE - 1) / VA_TILE + (window > 0 ? 1 : 0);
-    long long s = (tiles + 1) / 2;
+    long long s = (tiles + VA_MIN_SPLIT_TILES - 1) / VA_MIN_SPLIT_TILES;
     if (s > sm_count) s = sm_count;
     if (s < 1) s = 1;
     return (int)s;

@@ -130,8 +130,8 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 // A 4-byte load that asks L2 to fetch the whole 256-byte block around it (LSU path, not the TMA
 // engine); the value is discarded.
 __device__ __forceinline__ void touch_l2_256(const void* gaddr) {
-    uint32_t v;
-    asm volatile("ld.global.nc.L2::256B.b32 %0, [%1];" : "=r"(v) : "l"(reinterpret_cast<uint64_t>(gaddr)) : "memory");
+    uint32_t v = 0;
+    asm volatile("ld.global.nc.L2::256B.b32 %0, [%1];" : "+r"(v) : "l"(reinterpret_cast<uint64_t>(gaddr)) : "memory");
 }
 
 // Prefetch `bytes` (a multiple of 16) of contiguous global memory into L2.

@@ -82,9 +82,10 @@ def parse():
                     help="A/B comparison of two library builds on one GPU, alternated in ABBA BAAB order: each "
                          "argument is a comma-separated list of NAME=VALUE compile definitions ('' = the default "
                          "build); prints one JSON line with each build's per-block times and their spread")
-    ap.add_argument("--ab-what", choices=["call", "kernel"], default="call",
-                    help="A/B unit: a whole verify call (verify_attn_step, graph-replayed) or the split-attention "
-                         "launch alone (verify_attn_full, back to back)")
+    ap.add_argument("--ab-what", choices=["call", "kernel", "q8call", "q8"], default="call",
+                    help="A/B unit: a whole verify call (verify_attn_step, graph-replayed), the split-attention "
+                         "launch alone (verify_attn_full, back to back), or the same two over the quantised cache "
+                         "(verify_attn_q8_step / verify_attn_q8)")
     ap.add_argument("--ab-ctx", type=int, default=CTX, help="A/B workload context (positions)")
     ap.add_argument("--ab-window", type=int, default=0, help="A/B workload window (0 = full attention)")
     ap.add_argument("--ab-blocks", type=int, default=16, help="A/B timed blocks per build (a multiple of 4)")
@@ -1205,11 +1206,41 @@ def ab_compare(args, dist: Dist):
     S = max(arm["S"] for arm in arms.values())
     ws = torch.zeros(va.va_workspace_bytes(S) // 4, dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
+    quant = args.ab_what in ("q8", "q8call")
+    if quant:   # the same histories encoded into quantised caches by the library's encoder (build A's)
+        LA = arms["A"]["lib"]
+        for c in caches:
+            c["kc"] = torch.full((slots, 128), 0x7F, dtype=torch.uint8, device=dev)
+            c["vc"] = torch.zeros(slots, 128, dtype=torch.int8, device=dev)
+            c["ks"] = torch.full((slots,), float("nan"), device=dev)
+            c["vs"] = torch.full((slots,), float("nan"), device=dev)
+            first = max(0, ctx - slots) if window else 0
+            kh, vh = c["kb"][first:ctx].contiguous().to(dev), c["vb"][first:ctx].contiguous().to(dev)
+            hpos = torch.arange(first, ctx, dtype=torch.int32, device=dev)
+            st = LA.kv_ring_append_q8(P(kh.data_ptr()), P(vh.data_ptr()), ctx - first, P(c["kc"].data_ptr()),
+                                      P(c["vc"].data_ptr()), P(c["ks"].data_ptr()), P(c["vs"].data_ptr()), slots,
+                                      P(hpos.data_ptr()), None, sp)
+            if st:
+                raise RuntimeError(f"kv_ring_append_q8 failed with status {st}")
+            torch.cuda.synchronize(dev)
+            del kh, vh, hpos
 
     def launch(arm, x):
         L, S = arm["lib"], arm["S"]
         c = x["c"]
-        if args.ab_what == "call":
+        if args.ab_what == "q8call":
+            st = L.verify_attn_q8_step(P(c["q"].data_ptr()), P(x["kn"].data_ptr()), P(x["vn"].data_ptr()), 8, x["n"],
+                                       P(c["kc"].data_ptr()), P(c["vc"].data_ptr()), P(c["ks"].data_ptr()),
+                                       P(c["vs"].data_ptr()), slots, window, P(x["pos"].data_ptr()),
+                                       P(c["sink"].data_ptr()), ctypes.c_float(synth.SCALE), S, P(ws.data_ptr()),
+                                       P(x["out"].data_ptr()), None, None, P(status.data_ptr()), sp)
+        elif args.ab_what == "q8":
+            po = ws.data_ptr()
+            pl = po + 4 * S * 8 * 6 * 128
+            st = L.verify_attn_q8(P(c["q"].data_ptr()), 8, x["n"], P(c["kc"].data_ptr()), P(c["vc"].data_ptr()),
+                                  P(c["ks"].data_ptr()), P(c["vs"].data_ptr()), slots, window, P(x["pos"].data_ptr()),
+                                  ctypes.c_float(synth.SCALE), S, P(po), P(pl), None, P(status.data_ptr()), sp)
+        elif args.ab_what == "call":
             st = L.verify_attn_step(P(c["q"].data_ptr()), P(x["kn"].data_ptr()), P(x["vn"].data_ptr()), 8, x["n"],
                                     P(c["k"].data_ptr()), P(c["v"].data_ptr()), slots, window, P(x["pos"].data_ptr()),
                                     P(c["sink"].data_ptr()), ctypes.c_float(synth.SCALE), S, P(ws.data_ptr()),
@@ -1231,7 +1262,7 @@ def ab_compare(args, dist: Dist):
             for _ in range(3):
                 for x in calls:
                     launch(arm, x)
-            if args.ab_what == "call":
+            if args.ab_what in ("call", "q8call"):
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=stream):
                     for x in calls:
@@ -1240,23 +1271,23 @@ def ab_compare(args, dist: Dist):
         stream.synchronize()
         outs = {}
         for tag, arm in arms.items():   # both builds must compute the same thing
-            if args.ab_what == "call":
+            if args.ab_what in ("call", "q8call"):
                 graphs[tag].replay()
             else:
                 for x in calls:
                     launch(arm, x)
             stream.synchronize()
-            outs[tag] = torch.stack([x["out"].clone() for x in calls]) if args.ab_what == "call" else \
+            outs[tag] = torch.stack([x["out"].clone() for x in calls]) if args.ab_what in ("call", "q8call") else \
                 ws.clone()
         same = bool(torch.equal(outs["A"], outs["B"]))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         for tag in ab_order(max(4, args.ab_blocks)):
             arm = arms[tag]
-            if args.ab_what == "call":
+            if args.ab_what in ("call", "q8call"):
                 graphs[tag].replay()            # untimed: the block starts from a warm graph
             e0.record(stream)
             for _ in range(args.ab_reps):
-                if args.ab_what == "call":
+                if args.ab_what in ("call", "q8call"):
                     graphs[tag].replay()
                 else:
                     for x in calls:
@@ -1277,7 +1308,8 @@ def ab_compare(args, dist: Dist):
                       args.ab_reps * len(calls), "order": "ABBA BAAB", "A": res["A"], "B": res["B"],
                       "b_minus_a_us_median": statistics.median(d), "b_minus_a_us_min": min(d),
                       "b_minus_a_us_max": max(d), "outputs_identical": same,
-                      "unit": "us per verify call" if args.ab_what == "call" else "us per split-attention launch"}))
+                      "unit": "us per verify call" if args.ab_what in ("call", "q8call") else
+                      "us per split-attention launch"}))
 
 
 def main():

@@ -44,6 +44,13 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int rows, int box_rows)
 
 namespace q8 {
 
+// QK sums the three q terms in the tensor core (three N = 48 MMAs per k-step into one accumulator), so the
+// softmax warps read one 48-column score block; 0: one N = 144 MMA per k-step (each K slice read once) and
+// the three blocks added by the softmax warps.
+#ifndef VA_Q8_ACC3
+#define VA_Q8_ACC3 0
+#endif
+
 constexpr int kNK = 5;                     // K code ring depth (tiles of 128 positions); P' reuses K's stage
 constexpr int kNV = 3;                     // V code ring depth
 constexpr uint32_t kStage = 16384;         // 128 positions x 128 codes
@@ -406,7 +413,8 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             // QK: A = K codes, B = q terms, both E4M3 K-major; PV: A = V^T fp16, B = P'^T fp16, MN-major
-            constexpr uint32_t idesc_qk = (1u << 4) | (0u << 7) | (0u << 10) | ((144u >> 3) << 17) | ((128u >> 4) << 24);
+            constexpr uint32_t idesc_qk =
+                (1u << 4) | (0u << 7) | (0u << 10) | (((VA_Q8_ACC3 ? 48u : 144u) >> 3) << 17) | ((128u >> 4) << 24);
             constexpr uint32_t idesc_pv =
                 (1u << 4) | (0u << 7) | (0u << 10) | (1u << 15) | (1u << 16) | ((48u >> 3) << 17) | ((128u >> 4) << 24);
             // rotation: (H q)^T [128 x 48] = H . q^T into the first S buffer (A = H, B = q: bf16, K-major)
@@ -434,6 +442,20 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
                     const int ks = qk % kNK, sb = qk & 1;
                     ptx::tc_fence_after();
                     const uint32_t d = tmem + (sb ? kColS1 : kColS0);
+#if VA_Q8_ACC3
+                    // the three q terms (48 K-major rows, 6 KB each) accumulated into one block
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                        for (int t = 0; t < 3; ++t)
+                            asm volatile(
+                                "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                                " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+                                "l"(ptx::smem_desc(base_s + kOffK + ks * kStage + kk * 32, 0, 1024)),
+                                "l"(ptx::smem_desc(base_s + kOffQ + t * kQTerm + kk * 32, 0, 1024)), "r"(idesc_qk),
+                                "r"(kk > 0 || t > 0 ? 1u : 0u)
+                                : "memory");
+#else
                     // B = the three q terms as 144 consecutive K-major rows (each term 48 rows, 6 KB)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
@@ -444,6 +466,7 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
                             "l"(ptx::smem_desc(base_s + kOffQ + kk * 32, 0, 1024)), "r"(idesc_qk),
                             "r"(kk > 0 ? 1u : 0u)
                             : "memory");
+#endif
                     ptx::mma_commit(bar(ms.s_full[sb]));
                     ++qk;
                     progressed = true;
@@ -619,7 +642,7 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
                 float y[kCols];
                 ptx::tmem_ld24_wait(sc, x);
 #pragma unroll
-                for (int t = 1; t < 3; ++t) {
+                for (int t = 1; t < (VA_Q8_ACC3 ? 1 : 3); ++t) {
                     ptx::tmem_ld24_wait(sc + t * kTermCols, y);
 #pragma unroll
                     for (int i = 0; i < kCols; i += 2) {

@@ -27,8 +27,17 @@ constexpr float kLog2e = 1.4426950408889634f;
 // added in a fixed order: out = sum_s e^(lse_s - M) o_s / (sum_s e^(lse_s - M) + e^(sink - M)).  The
 // exponentials are the hardware exp2 of log2e-scaled differences (the library exp costs a dependent chain
 // of ~30 instructions per weight, which showed as ~1 us of the combine's time).
-template <int kCombineThreads, int kBatch>   // kBatch: splits per thread loaded together
-__global__ void __launch_bounds__(kCombineThreads) combine_kernel(const float* __restrict__ part_o,
+// Up to VA_COMBINE_SMALL splits (0: never), combine blocks of 128 threads at no more than 48 registers: small
+// enough to sit on an SM beside a split-attention CTA (which holds 168 x 352 of the SM's 65,536 registers), so
+// that the next call's split CTAs can start while this combine runs, and with 16 x 5 = 80 splits per load
+// batch still one round of loads.  Measured on GB300 per verify call: 1K 10.09 -> 9.34 us, the 4,103-position
+// window 10.72 -> 9.71 us; at 152 splits (two batches) +1.8 us, hence the bound.
+#ifndef VA_COMBINE_SMALL
+#define VA_COMBINE_SMALL 80
+#endif
+
+template <int kCombineThreads, int kBatch, int kMinBlocks = 1>   // kBatch: splits per thread loaded together
+__global__ void __launch_bounds__(kCombineThreads, kMinBlocks) combine_kernel(const float* __restrict__ part_o,
                                                                   const float* __restrict__ part_lse,
                                                                   int n_splits, const float* __restrict__ sink,
                                                                   int n_rows, int n_live,
@@ -138,6 +147,15 @@ cudaError_t launch_combine(const float* part_o, const float* part_lse, int n_spl
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     const bool wide = n_rows <= kMaxRows;
+#if VA_COMBINE_SMALL
+    if (wide && n_splits <= VA_COMBINE_SMALL) {
+        pdl_config(&cfg, attr, dim3(n_rows * kH, kQuarters), dim3(128), 0, stream);
+        __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, combine_kernel<128, 5, 10>, part_o, part_lse, n_splits, sink,
+                                                 n_rows, n_live, o, out_lse);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
+#endif
     pdl_config(&cfg, attr, dim3(n_rows * kH, kQuarters), dim3(wide ? 512 : 256), 0, stream);
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
     const cudaError_t e =

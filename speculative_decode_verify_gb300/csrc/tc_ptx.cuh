@@ -110,6 +110,12 @@ __device__ __forceinline__ int ld_int_policy(const int* gaddr, uint64_t policy) 
                  : "memory");
     return v;
 }
+// Relaxed load at GPU scope: a value another grid may be writing at the same time (no ordering implied).
+__device__ __forceinline__ int ld_relaxed_int(const int* gaddr) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(reinterpret_cast<uint64_t>(gaddr)) : "memory");
+    return v;
+}
 // 2-D tiled load with an L2 cache policy.
 __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
                                                  uint64_t policy) {

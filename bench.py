@@ -82,10 +82,10 @@ def parse():
                     help="A/B comparison of two library builds on one GPU, alternated in ABBA BAAB order: each "
                          "argument is a comma-separated list of NAME=VALUE compile definitions ('' = the default "
                          "build); prints one JSON line with each build's per-block times and their spread")
-    ap.add_argument("--ab-what", choices=["call", "kernel", "q8call", "q8"], default="call",
+    ap.add_argument("--ab-what", choices=["call", "kernel", "q8call", "q8", "tree"], default="call",
                     help="A/B unit: a whole verify call (verify_attn_step, graph-replayed), the split-attention "
                          "launch alone (verify_attn_full, back to back), or the same two over the quantised cache "
-                         "(verify_attn_q8_step / verify_attn_q8)")
+                         "(verify_attn_q8_step / verify_attn_q8), or a 16-node tree verify launch (verify_attn_tree)")
     ap.add_argument("--ab-ctx", type=int, default=CTX, help="A/B workload context (positions)")
     ap.add_argument("--ab-window", type=int, default=0, help="A/B workload window (0 = full attention)")
     ap.add_argument("--ab-blocks", type=int, default=16, help="A/B timed blocks per build (a multiple of 4)")
@@ -1201,10 +1201,17 @@ def ab_compare(args, dist: Dist):
                           vn=c["vb"][idx].contiguous().to(dev),
                           out=torch.empty(8, 6, 128, dtype=torch.int16, device=dev)))
     # each build picks its own split count (the split policy is one of the things an A/B may change)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     for arm in arms.values():
         arm["S"] = arm["lib"].va_auto_splits(window + 7 if window else slots, window)
+        if args.ab_what == "tree":   # two node groups share the SMs
+            arm["S"] = arm["lib"].va_auto_splits_for(window + 15 if window else slots, window, sms // 2)
+    if args.ab_what == "tree":
+        for i, c in enumerate(caches):
+            tw = synth.make_tree(f"abtree{i}", 980 + i, base=ctx - synth.TREE_NODES, n_nodes=synth.TREE_NODES)
+            c["tree"], c["tq"] = tw.tree.to(dev), synth.bits(tw.q).to(dev)
     S = max(arm["S"] for arm in arms.values())
-    ws = torch.zeros(va.va_workspace_bytes(S) // 4, dtype=torch.float32, device=dev)
+    ws = torch.zeros(2 * va.va_workspace_bytes(S) // 4, dtype=torch.float32, device=dev)   # room for 16 tree rows
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     quant = args.ab_what in ("q8", "q8call")
     if quant:   # the same histories encoded into quantised caches by the library's encoder (build A's)
@@ -1240,6 +1247,12 @@ def ab_compare(args, dist: Dist):
             st = L.verify_attn_q8(P(c["q"].data_ptr()), 8, x["n"], P(c["kc"].data_ptr()), P(c["vc"].data_ptr()),
                                   P(c["ks"].data_ptr()), P(c["vs"].data_ptr()), slots, window, P(x["pos"].data_ptr()),
                                   ctypes.c_float(synth.SCALE), S, P(po), P(pl), None, P(status.data_ptr()), sp)
+        elif args.ab_what == "tree":
+            po = ws.data_ptr()
+            pl = po + 4 * S * 16 * 6 * 128
+            st = L.verify_attn_tree(P(c["tq"].data_ptr()), 16, 16, P(c["k"].data_ptr()), P(c["v"].data_ptr()), slots,
+                                    window, P(c["tree"].data_ptr()), ctypes.c_float(synth.SCALE), S, P(po), P(pl),
+                                    None, P(status.data_ptr()), sp)
         elif args.ab_what == "call":
             st = L.verify_attn_step(P(c["q"].data_ptr()), P(x["kn"].data_ptr()), P(x["vn"].data_ptr()), 8, x["n"],
                                     P(c["k"].data_ptr()), P(c["v"].data_ptr()), slots, window, P(x["pos"].data_ptr()),

@@ -44,6 +44,13 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int rows, int box_rows)
 
 namespace q8 {
 
+// Tiles of a split pulled into L2 before the launch dependency resolves (0: none), as in the bf16 kernel.
+// Measured on GB300 at 192K: +0.4 us per launch and +2.7 us per verify_attn_q8_step call with 2 tiles
+// (+1.5 us at 1K), so off: this kernel's start is not where its time goes.
+#ifndef VA_PREWARM
+#define VA_PREWARM 0
+#endif
+
 // QK sums the three q terms in the tensor core (three N = 48 MMAs per k-step into one accumulator), so the
 // softmax warps read one 48-column score block; 0: one N = 144 MMA per k-step (each K slice read once) and
 // the three blocks added by the softmax warps.
@@ -272,7 +279,46 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
     }
 
     ptx::griddep_launch_dependents();
-    ptx::griddep_wait();   // every global access of this kernel comes after this
+#if VA_PREWARM
+    // a thread off the start's critical path pulls this split's first tiles (codes and row scales) into L2,
+    // and their address translations into the TLBs, while the kernel before may still run: from positions (or
+    // a tree descriptor) read now, a hint only (an L2 prefetch of the wrong lines costs bandwidth, never a
+    // result)
+    if (tid == 2 * 32 + 31 && n_live_g > 0) {   // lane 31 of the V producer warp: idle until the tail
+        Plan Q;
+        if (!is_tree) {
+            int sp[kMaxRows];
+#pragma unroll
+            for (int r = 0; r < kMaxRows; ++r) sp[r] = (r < a.n_live) ? ptx::ld_relaxed_int(a.pos + r) : 0;
+            Q = make_plan(sp, a.n_live, a.window, a.slots, a.n_splits, split);
+        } else {
+            int anc[kMaxNodes];
+#pragma unroll
+            for (int i = 0; i < kMaxNodes; ++i) anc[i] = (i < a.n_live) ? ptx::ld_relaxed_int(a.tree + 1 + i) : 0;
+            Q = make_tree_plan(ptx::ld_relaxed_int(a.tree), anc, a.n_live, a.window, a.slots, a.n_splits, split);
+        }
+        for (int j = 0; !Q.status && j < VA_PREWARM && Q.t0 + 2LL * j < Q.t1; ++j) {
+            const long long t = Q.t0 + 2LL * j;
+            const int halves = (t + 1 < Q.t1) ? 2 : 1;
+            const int s0 = (int)((t * kTile) % a.slots), s1 = (int)(((t + 1) * kTile) % a.slots);
+            if (halves == 2 && s1 == s0 + kTile) {
+                ptx::tma_prefetch_l2_2d(&tmk2, 0, s0);
+                ptx::tma_prefetch_l2_2d(&tmv2, 0, s0);
+            } else {
+                for (int hh = 0; hh < halves; ++hh) {
+                    ptx::tma_prefetch_l2_2d(&tmk, 0, hh ? s1 : s0);
+                    ptx::tma_prefetch_l2_2d(&tmv, 0, hh ? s1 : s0);
+                }
+            }
+            for (int hh = 0; hh < halves; ++hh) {
+                ptx::bulk_prefetch_l2(kscale_g + (hh ? s1 : s0), 256u);
+                ptx::bulk_prefetch_l2(vscale_g + (hh ? s1 : s0), 256u);
+            }
+        }
+    }
+#endif
+    ptx::griddep_wait();   // every global access of this kernel comes after this (the prefetches above only
+                           // pick lines for L2)
 
     // q first (two 48-row boxes, 128-byte swizzle, the B operand of the rotation) into the second fp16 V
     // buffer, which is idle until the second tile is widened; by thread 0, which initialised the barrier

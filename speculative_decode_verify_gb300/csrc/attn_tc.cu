@@ -81,6 +81,10 @@ namespace tc {
 #ifndef VA_PREWARM
 #define VA_PREWARM 2
 #endif
+// The same for draft trees (from the tree descriptor): measured ±0 on the 16-node tree at 192K, so off.
+#ifndef VA_PREWARM_TREE
+#define VA_PREWARM_TREE 0
+#endif
 constexpr int kNK = VA_NK;                // K ring depth (tiles of 128 positions); P of tile j reuses K's stage
 constexpr int kNV = VA_NV;                // V ring depth
 #ifndef VA_PREFETCH
@@ -278,20 +282,28 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
     if (warp == 1) ptx::tmem_alloc(ptx::smem_u32(&ms.tmem_base), kTmemCols);
     if (tid == 32) VA_TRACE_AT(241);
 
-#if VA_PREWARM
-    // a thread off the start's critical path warms L2 (and the address translations) for this split's first
-    // tiles while the kernel before may still run
-    if (!is_tree && tid == kThreads - 1 && n_live_g > 0) {
-        int sp[kMaxRows];
-#pragma unroll
-        for (int r = 0; r < kMaxRows; ++r) sp[r] = (r < a.n_live) ? ptx::ld_relaxed_int(a.pos + r) : 0;
-        const Plan Q = make_plan(sp, a.n_live, a.window, a.slots, a.n_splits, split);
-        if (!Q.status) prewarm_tiles(Q, VA_PREWARM, a.slots, &tmk, &tmk2, &tmv, &tmv2);
-    }
-#endif
     // Programmatic dependent launch: every global access of this kernel comes after griddep_wait (the
     // prefetches above only pick lines for L2).
     ptx::griddep_launch_dependents();
+#if VA_PREWARM
+    // a thread off the start's critical path warms L2 (and the address translations) for this split's first
+    // tiles while the kernel before may still run
+    if (tid == kThreads - 1 && n_live_g > 0 && (!is_tree || VA_PREWARM_TREE)) {
+        Plan Q;
+        if (!is_tree) {
+            int sp[kMaxRows];
+#pragma unroll
+            for (int r = 0; r < kMaxRows; ++r) sp[r] = (r < a.n_live) ? ptx::ld_relaxed_int(a.pos + r) : 0;
+            Q = make_plan(sp, a.n_live, a.window, a.slots, a.n_splits, split);
+        } else {
+            int anc[kMaxNodes];
+#pragma unroll
+            for (int i = 0; i < kMaxNodes; ++i) anc[i] = (i < a.n_live) ? ptx::ld_relaxed_int(a.tree + 1 + i) : 0;
+            Q = make_tree_plan(ptx::ld_relaxed_int(a.tree), anc, a.n_live, a.window, a.slots, a.n_splits, split);
+        }
+        if (!Q.status) prewarm_tiles(Q, VA_PREWARM, a.slots, &tmk, &tmk2, &tmv, &tmv2);
+    }
+#endif
     ptx::griddep_wait();
     if (tid == 0) VA_TRACE_AT(242);
 

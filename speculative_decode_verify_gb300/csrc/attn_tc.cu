@@ -81,6 +81,18 @@ namespace tc {
 #ifndef VA_PREWARM
 #define VA_PREWARM 2
 #endif
+// Speculative start of chain calls: the thread that warms L2 also requests tile 0 of the plan given by the
+// positions it read before the launch dependency resolved, as soon as it resolves, and only then reads the
+// positions again; if they differ (the kernel before was still writing them), it waits for those copies
+// and re-arms tile 0's barriers before any role uses them, and tile 0 is requested again with the rest.
+// VA_SPEC_SKEW (test builds only) shifts the early positions by one tile so that every launch whose tile 0
+// was requested early takes that path.
+#ifndef VA_SPEC
+#define VA_SPEC 0
+#endif
+#ifndef VA_SPEC_SKEW
+#define VA_SPEC_SKEW 0
+#endif
 // The same for draft trees (from the tree descriptor): measured ±0 on the 16-node tree at 192K, so off.
 #ifndef VA_PREWARM_TREE
 #define VA_PREWARM_TREE 0
@@ -137,7 +149,10 @@ struct Misc {
     Plan plan;                       // this split's extent and tiles (derived by warp 0)
     unsigned row_anc[kMaxRows];      // ancestor-or-self mask of each row of this CTA's group
     int pos[kMaxRows];
-    int anc[kMaxNodes];              // tree calls: every node's mask
+    int hint[kMaxRows];              // VA_SPEC: the positions as read before the launch dependency resolved
+    int spec_tile[3];                // VA_SPEC: tile 0 of the plan they give (halves, first slot, second slot)
+    int spec;                        // VA_SPEC: 2 when tile 0 was requested early from valid positions
+    int anc[kMaxNodes];              // tree calls: every node's mask              // tree calls: every node's mask
     int base;
 };
 constexpr uint32_t kSmemBytes = kOffMisc + (uint32_t)sizeof(Misc) + 1024;
@@ -166,6 +181,20 @@ __device__ __forceinline__ void prewarm_tiles(const Plan& Q, int n, int slots, c
                     ptx::tma_prefetch_l2_2d(v64, h * 64, hh ? s1 : s0);
                 }
         }
+    }
+}
+
+// The boxes of one K or V tile (those of load_tile): `halves` 64-row halves from slots s0 and s1.
+__device__ __forceinline__ void issue_tile(const CUtensorMap* m64, const CUtensorMap* m128, uint32_t stage,
+                                           uint32_t full, int halves, int s0, int s1) {
+    const uint64_t pol = ptx::policy_evict_first();
+    ptx::mbar_arrive_expect_tx(full, (uint32_t)halves * 2u * kHalfBox);
+    if (halves == 2 && s1 == s0 + kTile) {
+        for (int h = 0; h < 2; ++h) ptx::tma_load_2d_hint(stage + h * kDHalf, m128, h * 64, s0, full, pol);
+    } else {
+        for (int hh = 0; hh < halves; ++hh)
+            for (int h = 0; h < 2; ++h)
+                ptx::tma_load_2d_hint(stage + h * kDHalf + hh * kHalfBox, m64, h * 64, hh ? s1 : s0, full, pol);
     }
 }
 
@@ -269,9 +298,11 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
         ptx::mbar_init(bar(ms.drain), 1);
         if (kAppend) ptx::mbar_init(bar(ms.app_done), 1);
         ms.abort = 0;
+        if (VA_SPEC) ms.spec = 0;
         ptx::mbar_init_fence();
         VA_TRACE_AT(240);
     }
+    if (VA_SPEC && warp == 0) ptx::named_bar_arrive(2, 64);   // the barriers, to the early requester's warp
     if (tid == 32) {
         ptx::tma_prefetch_desc(&tmq);
         ptx::tma_prefetch_desc(&tmk);
@@ -285,7 +316,10 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
     // Programmatic dependent launch: every global access of this kernel comes after griddep_wait (the
     // prefetches above only pick lines for L2).
     ptx::griddep_launch_dependents();
-#if VA_PREWARM
+#if VA_SPEC
+    bool sp_planned = false;   // thread kThreads - 1: ms.hint and ms.spec_tile hold an early tile 0
+#endif
+#if VA_PREWARM || VA_SPEC
     // a thread off the start's critical path warms L2 (and the address translations) for this split's first
     // tiles while the kernel before may still run
     if (tid == kThreads - 1 && n_live_g > 0 && (!is_tree || VA_PREWARM_TREE)) {
@@ -293,19 +327,66 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
         if (!is_tree) {
             int sp[kMaxRows];
 #pragma unroll
-            for (int r = 0; r < kMaxRows; ++r) sp[r] = (r < a.n_live) ? ptx::ld_relaxed_int(a.pos + r) : 0;
+            for (int r = 0; r < kMaxRows; ++r)
+                sp[r] = (r < a.n_live) ? ptx::ld_relaxed_int(a.pos + r) - (VA_SPEC_SKEW ? kTile : 0) : 0;
             Q = make_plan(sp, a.n_live, a.window, a.slots, a.n_splits, split);
+#if VA_SPEC
+            const long long n64 = Q.t1 - Q.t0;
+            const int h0 = (n64 & 1) ? 1 : 2;
+            const bool new0 = kAppend && (long long)sp[0] < (Q.t0 + h0) * kTile && Q.hi > Q.t0 * kTile;
+            if (!Q.status && n64 > 0 && !new0) {   // (a tile 0 that holds new rows waits for the append)
+#pragma unroll
+                for (int r = 0; r < kMaxRows; ++r) ms.hint[r] = sp[r];
+                ms.spec_tile[0] = h0;
+                ms.spec_tile[1] = (int)((Q.t0 * kTile) % a.slots);
+                ms.spec_tile[2] = (int)(((Q.t0 + 1) * kTile) % a.slots);
+                sp_planned = true;
+            }
+#endif
         } else {
             int anc[kMaxNodes];
 #pragma unroll
             for (int i = 0; i < kMaxNodes; ++i) anc[i] = (i < a.n_live) ? ptx::ld_relaxed_int(a.tree + 1 + i) : 0;
             Q = make_tree_plan(ptx::ld_relaxed_int(a.tree), anc, a.n_live, a.window, a.slots, a.n_splits, split);
         }
-        if (!Q.status) prewarm_tiles(Q, VA_PREWARM, a.slots, &tmk, &tmk2, &tmv, &tmv2);
+        if (VA_PREWARM && !Q.status) prewarm_tiles(Q, VA_PREWARM, a.slots, &tmk, &tmk2, &tmv, &tmv2);
     }
 #endif
     ptx::griddep_wait();
     if (tid == 0) VA_TRACE_AT(242);
+#if VA_SPEC
+    if (warp == kThreads / 32 - 1) {
+        ptx::named_bar_sync(2, 64);   // thread 0's barrier initialisation is visible from here on
+        if (tid == kThreads - 1 && sp_planned) {
+            ms.t_first = ptx::globaltimer_ns();
+            VA_TRACE_TILE(0, 0);
+            issue_tile(&tmk, &tmk2, base_s + kOffK, bar(ms.k_full[0]), ms.spec_tile[0], ms.spec_tile[1], ms.spec_tile[2]);
+            VA_TRACE_TILE(0, 1);
+            issue_tile(&tmv, &tmv2, base_s + kOffV, bar(ms.v_full[0]), ms.spec_tile[0], ms.spec_tile[1], ms.spec_tile[2]);
+            int now[kMaxRows];
+#pragma unroll
+            for (int r = 0; r < kMaxRows; ++r) now[r] = (r < a.n_live) ? __ldcg(a.pos + r) : 0;
+            bool same = true;
+#pragma unroll
+            for (int r = 0; r < kMaxRows; ++r) same &= r >= a.n_live || now[r] == ms.hint[r];
+            if (same) {
+                ms.spec = 2;
+            } else if (ptx::mbar_wait(bar(ms.k_full[0]), 0, nullptr, kWaitNs) &&
+                       ptx::mbar_wait(bar(ms.v_full[0]), 0, nullptr, kWaitNs)) {
+                // a stale hint: its copies have landed; tile 0's barriers start over at phase 0
+                ptx::mbar_inval(bar(ms.k_full[0]));
+                ptx::mbar_init(bar(ms.k_full[0]), 1);
+                ptx::mbar_inval(bar(ms.v_full[0]));
+                ptx::mbar_init(bar(ms.v_full[0]), 1);
+                ptx::mbar_init_fence();
+            } else {   // never re-armed: nothing more is requested into it and every role gives up
+                ms.spec = 2;
+                ms.abort = 1;
+                if (a.dev_status) atomicOr(a.dev_status, VA_DEV_TIMEOUT);
+            }
+        }
+    }
+#endif
 
     // the positions (or the tree): one request per CTA; warp 0 derives the plan and shares it through
     // shared memory (the other warps would only compete with it for issue slots)
@@ -442,9 +523,14 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
                 ptx::tma_load_2d(base_s + kOffQ, &tmq, 0, kMaxM * group, bar(ms.q_full));
                 ptx::tma_load_2d(base_s + kOffQ + kQHalf, &tmq, 64, kMaxM * group, bar(ms.q_full));
             }
-            ms.t_first = ptx::globaltimer_ns();
-            for (int j = 0; j < k_first; ++j) load_k(j);
-            for (int j = 0; j < v_first; ++j) load_v(j);
+#if VA_SPEC
+            const int j0 = ms.spec == 2 ? 1 : 0;   // tile 0 requested early
+#else
+            constexpr int j0 = 0;
+#endif
+            if (!j0) ms.t_first = ptx::globaltimer_ns();
+            for (int j = j0; j < k_first; ++j) load_k(j);
+            for (int j = j0; j < v_first; ++j) load_v(j);
         }
         if (tid < kMaxRows) {
             // row tid of this group: the positions it sees inside this split, [lo, hi), and its mask of

@@ -125,11 +125,13 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
     return d;
 }
-// Value of an E4M3 code (sign, 4 exponent bits with bias 7, 3 mantissa bits), from the format.
-__device__ __forceinline__ float e4m3_to_float(uint32_t c) {
-    const uint32_t e = (c >> 3) & 15u, m = c & 7u;
-    const float mag = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0.001953125f;   // m 2^-9
-    return (c & 0x80u) ? -mag : mag;
+
+// Values of two E4M3 codes (lo in bits 0..7) by the hardware conversion to f16, which is exact.
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t c) {
+    float2 r;
+    asm("{\n .reg .b32 h;\n .reg .f16 lo, hi;\n cvt.rn.f16x2.e4m3x2 h, %2;\n mov.b32 {lo, hi}, h;\n"
+        " cvt.f32.f16 %0, lo;\n cvt.f32.f16 %1, hi;\n}" : "=f"(r.x), "=f"(r.y) : "h"((uint16_t)c));
+    return r;
 }
 
 // Four INT8 codes (one 32-bit word) to four exact fp16 values: 1152 + x is exact in fp16 for x in
@@ -599,8 +601,9 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
                     const uint32_t c = e4m3x2(r0, r1);
                     base[kOffQ + t * kQTerm + off0] = (unsigned char)(c & 0xFFu);
                     base[kOffQ + t * kQTerm + off1] = (unsigned char)(c >> 8);
-                    r0 -= e4m3_to_float(c & 0xFFu);   // exact: the residual of a rounding to 4 significant bits
-                    r1 -= e4m3_to_float(c >> 8);
+                    const float2 dq = e4m3x2_to_float2(c);
+                    r0 -= dq.x;   // exact: the residual of a rounding to 4 significant bits
+                    r1 -= dq.y;
                 }
             }
         }
@@ -633,8 +636,10 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
             // ch) into the fp16 buffer of this tile's parity once the PV two tiles back has read it; then the
             // code stage is free
             if (!ptx::mbar_wait(bar(ms.v_full[vs]), (j / kNV) & 1, abort_flag, kWaitNs)) ok = false;
-            const float sv = ms.vscale[vs][L];
             const bool own = L < nkeys && kp >= own_lo && kp < own_hi;
+            // keys outside the split's range keep the finite values their stale codes widen to (every byte is
+            // an INT8 code) and get P' = 0 through a zero V scale (their p is zero too)
+            const float sv = own ? ms.vscale[vs][L] : 0.0f;
             uint4 raw[4];
             {
                 const uint32_t roff = kOffV + (uint32_t)vs * kStage + (uint32_t)(L >> 3) * 1024u + (uint32_t)(L & 7) * 128u;
@@ -655,7 +660,6 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
                     int8x4_to_half(raw[c].y, h0.z, h0.w);
                     int8x4_to_half(raw[c].z, h1.x, h1.y);
                     int8x4_to_half(raw[c].w, h1.z, h1.w);
-                    if (!own) h0 = h1 = make_uint4(0u, 0u, 0u, 0u);
                     *reinterpret_cast<uint4*>(base + woff + (((uint32_t)(2 * c) ^ (uint32_t)(L & 7)) << 4)) = h0;
                     *reinterpret_cast<uint4*>(base + woff + (((uint32_t)(2 * c + 1) ^ (uint32_t)(L & 7)) << 4)) = h1;
                 }
@@ -785,7 +789,7 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
 #pragma unroll
             for (int i = 0; i < kCols / 2; ++i) {
                 const float2 s2 = mul2(make_float2(p[2 * i], p[2 * i + 1]), make_float2(sv, sv));
-                pw[i] = own ? pack_half2(s2.x, s2.y) : 0u;
+                pw[i] = pack_half2(s2.x, s2.y);
             }
             {
                 const uint32_t roff = kOffK + (uint32_t)ks * kStage + (uint32_t)(L >> 3) * 1024u + (uint32_t)(L & 7) * 128u;

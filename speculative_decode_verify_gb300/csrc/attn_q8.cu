@@ -73,15 +73,47 @@ constexpr uint32_t kOffMisc = kOffQ + 3 * kQTerm;
 constexpr uint32_t kOffH = kOffV16;              // +-1 Hadamard matrix, bf16 K-major (two 16 KB d halves)
 constexpr uint32_t kOffQStage = kOffV16 + kV16;  // q, bf16 K-major (two 6 KB d halves)
 constexpr uint32_t kQHalf16 = 6144;
-constexpr int kSoftWarps = 8;
+// Softmax / widening warps: 8 (two column halves of the 48 matrix rows, 24 columns a thread) or 16 (four
+// column quarters, 12 columns a thread, 96 registers).  Measured on GB300 at 192K: 16 warps +0.8 us per
+// launch, bit-identical: each step of a tile takes as long with half the work a warp (the exponentials
+// are bound by the MUFU pipe, 6,144 a tile and SM, and the rest by fixed latencies), so 8.
+#ifndef VA_Q8_SOFT_WARPS
+#define VA_Q8_SOFT_WARPS 8
+#endif
+constexpr int kSoftWarps = VA_Q8_SOFT_WARPS;
+static_assert(kSoftWarps == 8 || kSoftWarps == 16, "softmax warps: 8 or 16");
 constexpr int kSoftWarp0 = 3;
 constexpr int kThreads = 32 * (kSoftWarp0 + kSoftWarps);
 constexpr int kSoftThreads = 32 * kSoftWarps;
-constexpr int kCols = kMaxM / 2;
+constexpr int kColParts = kSoftWarps / 4;        // column parts: each lane quadrant has one warp per part
+constexpr int kCols = kMaxM / kColParts;         // matrix rows (accumulator columns) per softmax thread
+constexpr int kPartRows = kMaxRows / kColParts;  // verify rows per column part
+constexpr int kVChunks = 8 / kColParts;          // 16-code chunks of a V row widened per thread
 // S^T of a tile is three 48-column blocks, one per E4M3 term of q (QK runs as one N = 144 MMA per k-step,
-// so that each K slice is read once), double-buffered; then O^T (48 columns).
+// so that each K slice is read once), in VA_Q8_S_BUFS buffers; then O^T (48 columns).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0, kColS1 = 160, kColO = 320;
+// Order of a tile's steps in the softmax warps.  0: widen V, then the scores; 1: the scores' TMEM loads
+// first, then V's codes, and the widening in the same block of code as the exponentials, so that the
+// INT8 -> fp16 work (ALU, shared stores) fills the time the exponentials spend in the MUFU pipe.
+// Measured on GB300 at 192K (per launch, back to back, bit-identical): 1 alone -0.23 us; with three score
+// buffers (VA_Q8_S_BUFS) -0.94 us (19.67 -> 18.74 us); three buffers alone +0.09 us.
+#ifndef VA_Q8_FUSE
+#define VA_Q8_FUSE 1
+#endif
+// The per-tile vote on raising the reference maximum: 0 a block barrier of the softmax warps; 1 an mbarrier
+// (split phase): each warp arrives with its vote, writes P' as if no warp wanted a rescale, then waits and
+// rewrites P' in the rare tile that needs one.  Measured on GB300 at 192K: +0.03 us per launch, so 0.
+#ifndef VA_Q8_VOTE_MB
+#define VA_Q8_VOTE_MB 0
+#endif
+// VA_Q8_S_BUFS score buffers: QK may run that many tiles minus one ahead of PV (see VA_Q8_FUSE).
+#ifndef VA_Q8_S_BUFS
+#define VA_Q8_S_BUFS 3
+#endif
+constexpr int kSBufs = VA_Q8_S_BUFS;
+static_assert(kSBufs == 2 || kSBufs == 3, "score buffers: 2 or 3");
+constexpr uint32_t kSStride = kSBufs == 2 ? 160 : 144;   // TMEM columns between score buffers
+constexpr uint32_t kColS0 = 0, kColO = kSBufs * kSStride;
 constexpr uint32_t kTermCols = 48;
 constexpr float kThresh = 256.0f;
 constexpr float kRefInit = -1.0e30f;
@@ -89,7 +121,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 
 struct Misc {
     uint64_t k_full[kNK], k_empty[kNK], v_full[kNV], v_empty[kNV];
-    uint64_t q_tma, h_ready, q_rot, q_full, s_full[2], s_free[2], p_full[2], pv_done[2], o_ready, drain;
+    uint64_t q_tma, h_ready, q_rot, q_full, s_full[kSBufs], s_free[kSBufs], vote_bar[2], p_full[2], pv_done[2], o_ready, drain;
     uint32_t tmem_base;
     int abort;
     int vote[2][kSoftWarps];
@@ -177,14 +209,32 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     return u;
 }
 
-__device__ __forceinline__ int scatter_col_base(int lane) {
-    return ((lane >> 4) & 1) * 12 + ((lane >> 3) & 1) * 6 + ((lane >> 2) & 1) * 3;
+// This thread's kCols accumulator columns of its TMEM lane from taddr on, loaded (then waited for) or stored.
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[kCols]) {
+    if constexpr (kCols == 24) ptx::tmem_ld24_wait(taddr, v);
+    else ptx::tmem_ld12_wait(taddr, v);
+}
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const float (&v)[kCols]) {
+    if constexpr (kCols == 24) {
+        ptx::tmem_st16(taddr, v);
+        ptx::tmem_st8(taddr + 16, v + 16);
+    } else {
+        ptx::tmem_st8(taddr, v);
+        ptx::tmem_st4(taddr + 8, v + 8);
+    }
 }
 
-// Reduce 24 per-thread columns over the warp; afterwards the lane holds the warp totals of columns
+__device__ __forceinline__ int scatter_col_base(int lane) {
+    return kCols == 24 ? ((lane >> 4) & 1) * 12 + ((lane >> 3) & 1) * 6 + ((lane >> 2) & 1) * 3
+                       : ((lane >> 4) & 1) * 6 + ((lane >> 3) & 1) * 3;
+}
+// the lanes that hold distinct column totals after warp_reduce_scatter
+__device__ __forceinline__ bool scatter_writer(int lane) { return (lane & (kCols == 24 ? 3 : 7)) == 0; }
+
+// Reduce the kCols per-thread columns over the warp; afterwards the lane holds the warp totals of columns
 // [scatter_col_base(lane), +3) in v[0..2].
 template <bool kMax>
-__device__ __forceinline__ void warp_reduce_scatter24(float (&v)[kCols], int lane) {
+__device__ __forceinline__ void warp_reduce_scatter(float (&v)[kCols], int lane) {
 #define VA_STAGE(W, BIT)                                                   \
     _Pragma("unroll") for (int i = 0; i < (W); ++i) {                      \
         const bool up = (lane & (BIT)) != 0;                               \
@@ -193,12 +243,14 @@ __device__ __forceinline__ void warp_reduce_scatter24(float (&v)[kCols], int lan
         const float got = __shfl_xor_sync(0xffffffffu, send, (BIT));       \
         v[i] = kMax ? fmaxf(keep, got) : keep + got;                       \
     }
-    VA_STAGE(12, 16)
-    VA_STAGE(6, 8)
-    VA_STAGE(3, 4)
+    VA_STAGE(kCols / 2, 16)
+    VA_STAGE(kCols / 4, 8)
+    if (kCols == 24) {
+        VA_STAGE(3, 4)
+    }
 #undef VA_STAGE
 #pragma unroll
-    for (int b = 2; b >= 1; b >>= 1)
+    for (int b = kCols == 24 ? 2 : 4; b >= 1; b >>= 1)
 #pragma unroll
         for (int i = 0; i < 3; ++i) {
             const float got = __shfl_xor_sync(0xffffffffu, v[i], b);
@@ -239,9 +291,12 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
             ptx::mbar_init(bar(ms.v_full[i]), 1);
             ptx::mbar_init(bar(ms.v_empty[i]), kSoftWarps);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kSBufs; ++i) {
             ptx::mbar_init(bar(ms.s_full[i]), 1);
             ptx::mbar_init(bar(ms.s_free[i]), kSoftWarps);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(bar(ms.vote_bar[i]), kSoftWarps);
             ptx::mbar_init(bar(ms.p_full[i]), kSoftWarps);
             ptx::mbar_init(bar(ms.pv_done[i]), 1);
         }
@@ -260,12 +315,14 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
     if (warp == 1) ptx::tmem_alloc(ptx::smem_u32(&ms.tmem_base), kTmemCols);
     // the +-1 Hadamard matrix H[i][j] = (-1)^popcount(i & j) as the bf16 A operand of the rotation, written
     // by the softmax warps before the dependency wait (it needs no global memory): thread st writes row
-    // st & 127, d half st >> 7 (eight 16-byte chunks of 8 entries, 128-byte swizzle)
+    // st & 127, d half (st >> 7) & 1, kHChunks of its eight 16-byte chunks of 8 entries (128-byte swizzle)
     if (warp >= kSoftWarp0) {
-        const int st = (warp - kSoftWarp0) * 32 + lane, row = st & 127, h = st >> 7;
+        constexpr int kHChunks = 8 * 256 / kSoftThreads;
+        const int st = (warp - kSoftWarp0) * 32 + lane, row = st & 127, h = (st >> 7) & 1;
+        const int c0 = (st >> 8) * kHChunks;
         const uint32_t roff = kOffH + (uint32_t)h * 16384u + (uint32_t)(row >> 3) * 1024u + (uint32_t)(row & 7) * 128u;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = c0; c < c0 + kHChunks; ++c) {
             uint32_t w[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -484,12 +541,12 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
             uint64_t idle_since = 0;
             while (ok && pv < ntiles) {
                 bool progressed = false;
-                if (qk < ntiles && qk <= pv + 1 &&
+                if (qk < ntiles && qk <= pv + kSBufs - 1 &&
                     ptx::mbar_test_wait(bar(ms.k_full[qk % kNK]), (qk / kNK) & 1) &&
-                    ptx::mbar_test_wait(bar(ms.s_free[qk & 1]), ((qk >> 1) & 1) ^ 1)) {
-                    const int ks = qk % kNK, sb = qk & 1;
+                    ptx::mbar_test_wait(bar(ms.s_free[qk % kSBufs]), ((qk / kSBufs) & 1) ^ 1)) {
+                    const int ks = qk % kNK, sb = qk % kSBufs;
                     ptx::tc_fence_after();
-                    const uint32_t d = tmem + (sb ? kColS1 : kColS0);
+                    const uint32_t d = tmem + kColS0 + (uint32_t)sb * kSStride;
 #if VA_Q8_ACC3
                     // the three q terms (48 K-major rows, 6 KB each) accumulated into one block
 #pragma unroll
@@ -560,19 +617,19 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
 
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(bar(ms.h_ready));   // H was written before the dependency wait
-        // (H q)^T: thread L holds rotated element d' = L of rows n0 .. n0 + 23.  Per row, a power of two
+        // (H q)^T: thread L holds rotated element d' = L of rows n0 .. n0 + kCols - 1.  Per row, a power of two
         // s_r brings the largest element into [128, 256); the scaled row splits into three E4M3 terms.
         if (!ptx::mbar_wait(bar(ms.q_rot), 0, abort_flag, kWaitNs)) ok = false;
         ptx::tc_fence_after();
         {
             float hq[kCols];
-            ptx::tmem_ld24_wait(tl + kColS0 + n0, hq);
+            tmem_ld_cols(tl + kColS0 + n0, hq);
             float m[kCols];
 #pragma unroll
             for (int i = 0; i < kCols; ++i) m[i] = fabsf(hq[i]);
-            warp_reduce_scatter24<true>(m, lane);
+            warp_reduce_scatter<true>(m, lane);
             const int cb = n0 + scatter_col_base(lane);
-            if ((lane & 3) == 0) {
+            if (scatter_writer(lane)) {
                 ms.red[q][cb] = m[0];
                 ms.red[q][cb + 1] = m[1];
                 ms.red[q][cb + 2] = m[2];
@@ -631,52 +688,61 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
             const int nkeys = (t + 1 < P.t1) ? 128 : 64;
             const long long kbase = t * kTile;
             const long long kp = kbase + L;
-            const int sb = j & 1, ks = j % kNK, vs = j % kNV;
-            // V of this tile first, while QK(j) runs: its scales, then its codes widened to fp16 (key L, d half
-            // ch) into the fp16 buffer of this tile's parity once the PV two tiles back has read it; then the
-            // code stage is free
-            if (!ptx::mbar_wait(bar(ms.v_full[vs]), (j / kNV) & 1, abort_flag, kWaitNs)) ok = false;
+            const int sb = j % kSBufs, ks = j % kNK, vs = j % kNV;
             const bool own = L < nkeys && kp >= own_lo && kp < own_hi;
-            // keys outside the split's range keep the finite values their stale codes widen to (every byte is
-            // an INT8 code) and get P' = 0 through a zero V scale (their p is zero too)
-            const float sv = own ? ms.vscale[vs][L] : 0.0f;
-            uint4 raw[4];
-            {
+            // V: its scales, then its codes (key L, the d range of column part ch), widened to fp16 into the
+            // buffer of this tile's parity once the PV two tiles back has read it; the code stage is free as
+            // soon as the codes are in registers.  Keys outside the split's range keep the finite values their
+            // stale codes widen to (every byte is an INT8 code) and get P' = 0 through a zero V scale (their p
+            // is zero too).
+            float sv;
+            uint4 raw[kVChunks];
+            auto read_v = [&]() {
+                if (!ptx::mbar_wait(bar(ms.v_full[vs]), (j / kNV) & 1, abort_flag, kWaitNs)) ok = false;
+                sv = own ? ms.vscale[vs][L] : 0.0f;
                 const uint32_t roff = kOffV + (uint32_t)vs * kStage + (uint32_t)(L >> 3) * 1024u + (uint32_t)(L & 7) * 128u;
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    raw[c] = *reinterpret_cast<const uint4*>(base + roff + (((uint32_t)(4 * ch + c) ^ (uint32_t)(L & 7)) << 4));
-            }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bar(ms.v_empty[vs]));
-            if (j >= 2 && !ptx::mbar_wait(bar(ms.pv_done[j & 1]), ((j - 2) >> 1) & 1, abort_flag, kWaitNs)) ok = false;
-            {
-                const uint32_t woff = kOffV16 + (uint32_t)(j & 1) * kV16 + (uint32_t)ch * kV16Half +
+                for (int c = 0; c < kVChunks; ++c)
+                    raw[c] = *reinterpret_cast<const uint4*>(
+                        base + roff + (((uint32_t)(kVChunks * ch + c) ^ (uint32_t)(L & 7)) << 4));
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(ms.v_empty[vs]));
+                if (j >= 2 && !ptx::mbar_wait(bar(ms.pv_done[j & 1]), ((j - 2) >> 1) & 1, abort_flag, kWaitNs)) ok = false;
+            };
+            auto widen = [&]() {
+                // d = kVChunks * 16 * ch + 16 c + ...: d half (64 values, one 128-byte row per key) and the
+                // 16-byte fp16 chunk inside it
+                const int dh = (kVChunks * ch) >> 2, k0 = 2 * ((kVChunks * ch) & 3);
+                const uint32_t woff = kOffV16 + (uint32_t)(j & 1) * kV16 + (uint32_t)dh * kV16Half +
                                       (uint32_t)(L >> 3) * 1024u + (uint32_t)(L & 7) * 128u;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int c = 0; c < kVChunks; ++c) {
                     uint4 h0, h1;   // 16 codes -> two 16-byte chunks of 8 fp16 values
                     int8x4_to_half(raw[c].x, h0.x, h0.y);
                     int8x4_to_half(raw[c].y, h0.z, h0.w);
                     int8x4_to_half(raw[c].z, h1.x, h1.y);
                     int8x4_to_half(raw[c].w, h1.z, h1.w);
-                    *reinterpret_cast<uint4*>(base + woff + (((uint32_t)(2 * c) ^ (uint32_t)(L & 7)) << 4)) = h0;
-                    *reinterpret_cast<uint4*>(base + woff + (((uint32_t)(2 * c + 1) ^ (uint32_t)(L & 7)) << 4)) = h1;
+                    *reinterpret_cast<uint4*>(base + woff + (((uint32_t)(k0 + 2 * c) ^ (uint32_t)(L & 7)) << 4)) = h0;
+                    *reinterpret_cast<uint4*>(base + woff + (((uint32_t)(k0 + 2 * c + 1) ^ (uint32_t)(L & 7)) << 4)) = h1;
                 }
+            };
+            if (!VA_Q8_FUSE) {
+                read_v();
+                widen();
             }
-            // which of the rows of this column half see key L (no score needed)
+            // which of the rows of this column part see key L (no score needed)
             const bool interior = kbase >= all_lo && kbase + nkeys <= all_hi;
             bool vis[kCols];
             {
-                bool rv[kMaxRows / 2];
+                bool rv[kPartRows];
                 if (interior) {
 #pragma unroll
-                    for (int k = 0; k < kMaxRows / 2; ++k) rv[k] = L < nkeys;
+                    for (int k = 0; k < kPartRows; ++k) rv[k] = L < nkeys;
                 } else {
                     const long long dk = kp - ms.tree_base;   // node index of key kp in a tree's node region
 #pragma unroll
-                    for (int k = 0; k < kMaxRows / 2; ++k) {
-                        const int r = (kMaxRows / 2) * ch + k;
+                    for (int k = 0; k < kPartRows; ++k) {
+                        const int r = kPartRows * ch + k;
                         const bool in_mask = dk < 0 || (dk < 32 && ((ms.row_anc[r] >> (int)dk) & 1u));
                         rv[k] = (r < n_live_g) && kp >= ms.row_lo[r] && kp < ms.row_hi[r] && in_mask;
                     }
@@ -684,21 +750,35 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
 #pragma unroll
                 for (int i = 0; i < kCols; ++i) vis[i] = rv[i / kH];
             }
-            if (!ptx::mbar_wait(bar(ms.s_full[sb]), (j >> 1) & 1, abort_flag, kWaitNs)) ok = false;
+            if (!ptx::mbar_wait(bar(ms.s_full[sb]), (j / kSBufs) & 1, abort_flag, kWaitNs)) ok = false;
             ptx::tc_fence_after();
             float x[kCols];
             {   // the three terms' scores, added
-                const uint32_t sc = tl + (sb ? kColS1 : kColS0) + n0;
-                float y[kCols];
-                ptx::tmem_ld24_wait(sc, x);
-#pragma unroll
-                for (int t = 1; t < (VA_Q8_ACC3 ? 1 : 3); ++t) {
-                    ptx::tmem_ld24_wait(sc + t * kTermCols, y);
+                const uint32_t sc = tl + kColS0 + (uint32_t)sb * kSStride + n0;
+                if (VA_Q8_ACC3) {
+                    tmem_ld_cols(sc, x);
+                } else if constexpr (kCols == 12) {   // all three terms in flight together: (x + y) + z
+                    float y[kCols], z[kCols];
+                    ptx::tmem_ld12x3_wait(sc, kTermCols, x, y, z);
 #pragma unroll
                     for (int i = 0; i < kCols; i += 2) {
-                        const float2 s2 = add2(make_float2(x[i], x[i + 1]), make_float2(y[i], y[i + 1]));
+                        const float2 s2 = add2(add2(make_float2(x[i], x[i + 1]), make_float2(y[i], y[i + 1])),
+                                               make_float2(z[i], z[i + 1]));
                         x[i] = s2.x;
                         x[i + 1] = s2.y;
+                    }
+                } else {
+                    float y[kCols];
+                    tmem_ld_cols(sc, x);
+#pragma unroll
+                    for (int t = 1; t < 3; ++t) {
+                        tmem_ld_cols(sc + t * kTermCols, y);
+#pragma unroll
+                        for (int i = 0; i < kCols; i += 2) {
+                            const float2 s2 = add2(make_float2(x[i], x[i + 1]), make_float2(y[i], y[i + 1]));
+                            x[i] = s2.x;
+                            x[i + 1] = s2.y;
+                        }
                     }
                 }
             }
@@ -722,6 +802,7 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
 #pragma unroll
                 for (int i = 0; i < kCols; ++i) ref[i] = ms.ref[n0 + i];
             }
+            if (VA_Q8_FUSE) read_v();
             float p[kCols];
             float pmax = 0.0f;
 #pragma unroll
@@ -732,9 +813,42 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
                 p[i + 1] = vis[i + 1] ? ptx::ex2(e2.y) : 0.0f;
                 pmax = fmaxf(pmax, fmaxf(p[i], p[i + 1]));
             }
+            if (VA_Q8_FUSE) widen();
+            // P' = p * v_scale as fp16, over this tile's K codes (QK(j) has read them)
+            auto store_p = [&]() {
+                uint32_t pw[kCols / 2];
+#pragma unroll
+                for (int i = 0; i < kCols / 2; ++i) {
+                    const float2 s2 = mul2(make_float2(p[2 * i], p[2 * i + 1]), make_float2(sv, sv));
+                    pw[i] = pack_half2(s2.x, s2.y);
+                }
+                const uint32_t roff = kOffK + (uint32_t)ks * kStage + (uint32_t)(L >> 3) * 1024u + (uint32_t)(L & 7) * 128u;
+                if constexpr (kCols == 24) {   // 48 bytes from byte 48 ch: three 16-byte chunks
+#pragma unroll
+                    for (int k = 0; k < 3; ++k) {
+                        const uint32_t off = roff + ((uint32_t)((3 * ch + k) ^ (L & 7)) << 4);
+                        *reinterpret_cast<uint4*>(base + off) = make_uint4(pw[4 * k], pw[4 * k + 1], pw[4 * k + 2], pw[4 * k + 3]);
+                    }
+                } else {   // 24 bytes from byte 24 ch: three 8-byte pieces
+#pragma unroll
+                    for (int k = 0; k < 3; ++k) {
+                        const uint32_t b = 24u * (uint32_t)ch + 8u * (uint32_t)k;
+                        const uint32_t off = roff + ((((b >> 4) ^ (uint32_t)(L & 7))) << 4) + (b & 15u);
+                        *reinterpret_cast<uint2*>(base + off) = make_uint2(pw[2 * k], pw[2 * k + 1]);
+                    }
+                }
+            };
             const unsigned want = __any_sync(0xffffffffu, !(pmax <= kThresh));
-            if (lane == 0) ms.vote[j & 1][sw] = want ? 1 : 0;
-            ptx::named_bar_sync(1, kSoftThreads);
+            if (lane == 0) {
+                ms.vote[j & 1][sw] = want ? 1 : 0;
+                if (VA_Q8_VOTE_MB) ptx::mbar_arrive(bar(ms.vote_bar[j & 1]));
+            }
+            if (VA_Q8_VOTE_MB) {
+                store_p();
+                if (!ptx::mbar_wait(bar(ms.vote_bar[j & 1]), (j >> 1) & 1, abort_flag, kWaitNs)) ok = false;
+            } else {
+                ptx::named_bar_sync(1, kSoftThreads);
+            }
             int any = 0;
 #pragma unroll
             for (int w = 0; w < kSoftWarps; ++w) any |= ms.vote[j & 1][w];
@@ -744,9 +858,9 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
                 float v[kCols];
 #pragma unroll
                 for (int i = 0; i < kCols; ++i) v[i] = vis[i] ? x[i] * cq[i] : -INFINITY;
-                warp_reduce_scatter24<true>(v, lane);
+                warp_reduce_scatter<true>(v, lane);
                 const int cb = n0 + scatter_col_base(lane);
-                if ((lane & 3) == 0) {
+                if (scatter_writer(lane)) {
                     ms.red[q][cb] = v[0];
                     ms.red[q][cb + 1] = v[1];
                     ms.red[q][cb + 2] = v[2];
@@ -769,13 +883,13 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
                 if (j > 0) {
                     ptx::tc_fence_after();
                     float o[kCols];
-                    ptx::tmem_ld24_wait(tl + kColO + n0, o);
+                    tmem_ld_cols(tl + kColO + n0, o);
 #pragma unroll
                     for (int i = 0; i < kCols; ++i) o[i] *= ms.alpha[n0 + i];
-                    ptx::tmem_st16(tl + kColO + n0, o);
-                    ptx::tmem_st8(tl + kColO + n0 + 16, o + 16);
+                    tmem_st_cols(tl + kColO + n0, o);
                     ptx::tmem_wait_st();
                 }
+                if (VA_Q8_VOTE_MB) store_p();
             }
 #pragma unroll
             for (int i = 0; i < kCols; i += 2) {
@@ -784,31 +898,17 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
                 l[i + 1] = s2.y;
             }
 
-            // P' = p * v_scale as fp16, over this tile's K codes (QK(j) has read them)
-            uint32_t pw[kCols / 2];
-#pragma unroll
-            for (int i = 0; i < kCols / 2; ++i) {
-                const float2 s2 = mul2(make_float2(p[2 * i], p[2 * i + 1]), make_float2(sv, sv));
-                pw[i] = pack_half2(s2.x, s2.y);
-            }
-            {
-                const uint32_t roff = kOffK + (uint32_t)ks * kStage + (uint32_t)(L >> 3) * 1024u + (uint32_t)(L & 7) * 128u;
-#pragma unroll
-                for (int k = 0; k < 3; ++k) {
-                    const uint32_t off = roff + ((uint32_t)((3 * ch + k) ^ (L & 7)) << 4);
-                    *reinterpret_cast<uint4*>(base + off) = make_uint4(pw[4 * k], pw[4 * k + 1], pw[4 * k + 2], pw[4 * k + 3]);
-                }
-            }
+            if (!VA_Q8_VOTE_MB) store_p();
             ptx::fence_proxy_async_smem();
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bar(ms.p_full[j & 1]));
         }
         // ------------------------------------------------------------ epilogue
-        warp_reduce_scatter24<false>(l, lane);
+        warp_reduce_scatter<false>(l, lane);
         {
             const int cb = n0 + scatter_col_base(lane);
-            if ((lane & 3) == 0) {
+            if (scatter_writer(lane)) {
                 ms.red[q][cb] = l[0];
                 ms.red[q][cb + 1] = l[1];
                 ms.red[q][cb + 2] = l[2];
@@ -824,7 +924,7 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
         if (!ptx::mbar_wait(bar(ms.o_ready), 0, abort_flag, kWaitNs)) ok = false;
         ptx::tc_fence_after();
         float o[kCols];
-        ptx::tmem_ld24_wait(tl + kColO + n0, o);
+        tmem_ld_cols(tl + kColO + n0, o);
 #pragma unroll
         for (int i = 0; i < kCols; ++i) {
             const int n = n0 + i;

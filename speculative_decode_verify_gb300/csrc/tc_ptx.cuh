@@ -247,6 +247,56 @@ __device__ __forceinline__ void tmem_ld24_wait(uint32_t taddr, float* v) {
     for (int i = 0; i < 24; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 12 consecutive columns (an 8- and a 4-column load in flight together), then the wait.
+__device__ __forceinline__ void tmem_ld12_wait(uint32_t taddr, float* v) {
+    uint32_t r[12];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%12];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%8,%9,%10,%11}, [%13];\n"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11])
+        : "r"(taddr), "r"(taddr + 8u)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 12; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Three blocks of 12 consecutive columns at taddr, taddr + gap and taddr + 2 gap (six loads in flight
+// together), then the wait.
+__device__ __forceinline__ void tmem_ld12x3_wait(uint32_t taddr, uint32_t gap, float* a, float* b, float* c) {
+    uint32_t r[36];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%36];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%8,%9,%10,%11}, [%37];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%12,%13,%14,%15,%16,%17,%18,%19}, [%38];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%20,%21,%22,%23}, [%39];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%24,%25,%26,%27,%28,%29,%30,%31}, [%40];\n"
+        "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%32,%33,%34,%35}, [%41];\n"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+          "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+          "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]),
+          "=r"(r[33]), "=r"(r[34]), "=r"(r[35])
+        : "r"(taddr), "r"(taddr + 8u), "r"(taddr + gap), "r"(taddr + gap + 8u), "r"(taddr + 2u * gap),
+          "r"(taddr + 2u * gap + 8u)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 12; ++i) {
+        a[i] = __uint_as_float(r[i]);
+        b[i] = __uint_as_float(r[12 + i]);
+        c[i] = __uint_as_float(r[24 + i]);
+    }
+}
+
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const float* v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr),
+                 "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                 "r"(__float_as_uint(v[3]))
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const float* v) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
                  "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),

@@ -82,7 +82,7 @@ def parse():
                     help="A/B comparison of two library builds on one GPU, alternated in ABBA BAAB order: each "
                          "argument is a comma-separated list of NAME=VALUE compile definitions ('' = the default "
                          "build); prints one JSON line with each build's per-block times and their spread")
-    ap.add_argument("--ab-what", choices=["call", "kernel", "q8call", "q8", "tree"], default="call",
+    ap.add_argument("--ab-what", choices=["call", "kernel", "q8call", "q8", "tree", "sample"], default="call",
                     help="A/B unit: a whole verify call (verify_attn_step, graph-replayed), the split-attention "
                          "launch alone (verify_attn_full, back to back), or the same two over the quantised cache "
                          "(verify_attn_q8_step / verify_attn_q8), or a 16-node tree verify launch (verify_attn_tree)")
@@ -1193,6 +1193,8 @@ def ab_compare(args, dist: Dist):
     stream = torch.cuda.Stream(dev)
     sp = ctypes.c_void_p(stream.cuda_stream)
     P = ctypes.c_void_p
+    if args.ab_what == "sample":
+        return ab_sample(args, arms, dev, stream, sp)
     ctx, window = args.ab_ctx, args.ab_window
     slots = synth.RING_SLOTS if window else ctx + 64
     n_caches = 5 if 512 * ctx > (32 << 20) else 2
@@ -1338,6 +1340,75 @@ def ab_compare(args, dist: Dist):
                       "b_minus_a_us_max": max(d), "outputs_identical": same,
                       "unit": "us per verify call" if args.ab_what in ("call", "q8call") else
                       "us per split-attention launch"}))
+
+
+def ab_sample(args, arms, dev, stream, sp):
+    """A/B of va_sample_topk_topp: 8 rows x 160,000 logits, top-k 20 / top-p 0.95, 32 rotating logit
+    buffers (read cold), 16 calls per CUDA graph."""
+    import ctypes
+
+    import torch
+
+    import speculative_decode_verify_gb300 as va
+    from speculative_decode_verify_gb300 import synth
+
+    P = ctypes.c_void_p
+    n, vocab, k = 8, synth.VOCAB, 20
+    xs = [synth.logits(700 + i, n).to(dev) for i in range(32)]
+    u = synth.uniforms(7, n).to(dev)
+    wsb = va.va_sample_workspace_bytes(n, vocab, k)
+    for arm in arms.values():
+        arm["ws"] = torch.zeros(wsb, dtype=torch.uint8, device=dev)
+        arm["outs"] = [torch.empty(n * k, dtype=torch.int32, device=dev), torch.empty(n * k, device=dev),
+                       torch.empty(n, dtype=torch.int32, device=dev), torch.empty(n, dtype=torch.int32, device=dev)]
+    per_graph = 16
+
+    def launch(arm, x):
+        o = arm["outs"]
+        st = arm["lib"].va_sample_topk_topp(P(x.data_ptr()), n, vocab, k, ctypes.c_float(0.95), ctypes.c_float(1.0),
+                                            P(u.data_ptr()), P(o[0].data_ptr()), P(o[1].data_ptr()), P(o[2].data_ptr()),
+                                            P(o[3].data_ptr()), P(arm["ws"].data_ptr()), wsb, sp)
+        if st:
+            raise RuntimeError(f"A/B sample launch failed with status {st}")
+
+    with torch.cuda.stream(stream):
+        graphs, outs = {}, {}
+        for tag, arm in arms.items():
+            for i in range(3):
+                launch(arm, xs[i])
+            launch(arm, xs[5])
+            stream.synchronize()
+            outs[tag] = [t.clone() for t in arm["outs"]]
+            gs = []
+            for g0 in range(2):   # two graphs over different buffers: every call reads logits not in L2
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for i in range(per_graph):
+                        launch(arm, xs[g0 * per_graph + i])
+                gs.append(g)
+            graphs[tag] = gs
+        stream.synchronize()
+        same = all(torch.equal(a, b) for a, b in zip(outs["A"], outs["B"]))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for tag in ab_order(max(4, args.ab_blocks)):
+            arm = arms[tag]
+            graphs[tag][1].replay()
+            e0.record(stream)
+            for r in range(args.ab_reps):
+                graphs[tag][r & 1].replay()
+            e1.record(stream)
+            e1.synchronize()
+            arm["times"].append(e0.elapsed_time(e1) * 1e3 / (args.ab_reps * per_graph))
+    res = {}
+    for tag, arm in arms.items():
+        t = arm["times"]
+        res[tag] = {"defines": arm["spec"], "us_median": statistics.median(t), "us_min": min(t), "us_max": max(t),
+                    "us_stdev": statistics.stdev(t) if len(t) > 1 else 0.0, "blocks": [round(x, 3) for x in t]}
+    d = [b - a for a, b in zip(arms["A"]["times"], arms["B"]["times"])]
+    print(json.dumps({"ab": "sample", "rows": n, "vocab": vocab, "top_k": k, "calls_per_block": args.ab_reps * per_graph,
+                      "order": "ABBA BAAB", "A": res["A"], "B": res["B"], "b_minus_a_us_median": statistics.median(d),
+                      "b_minus_a_us_min": min(d), "b_minus_a_us_max": max(d), "outputs_identical": same,
+                      "unit": "us per sampling call"}))
 
 
 def main():

@@ -93,6 +93,17 @@ namespace tc {
 #ifndef VA_SPEC_SKEW
 #define VA_SPEC_SKEW 0
 #endif
+// Start: 0 two block barriers after the launch dependency (warp 0's plan, then the set-up); 1 one block
+// barrier before it (barriers and TMEM), a named barrier on which warp 0 only arrives once its plan is
+// published (it then requests q and the first K stages at once), the V producer requesting its own first
+// stages, and the row set-up by the softmax warps behind their own barrier.  Measured on GB300 (per
+// verify call, outputs bit-identical): 1K 9.30 -> 8.62 us, the 4,103-position window 9.61 -> 8.92 us,
+// 192K 24.03 -> 23.83 us; the split launch alone back to back and the 16-node tree within 0.1 us.  (The row
+// set-up by warp 0 behind a third named barrier: -0.64, -0.67 and -0.10 us.)
+#ifndef VA_EARLY
+#define VA_EARLY 1
+#endif
+static_assert(!(VA_EARLY && VA_SPEC), "the speculative start assumes the two-barrier start");
 // The same for draft trees (from the tree descriptor): measured ±0 on the 16-node tree at 192K, so off.
 #ifndef VA_PREWARM_TREE
 #define VA_PREWARM_TREE 0
@@ -138,6 +149,7 @@ struct Misc {
     uint64_t app_done;               // verify_attn_step: this split's share of the append is written
     uint32_t tmem_base;
     int abort;
+    unsigned long long t_first_v;    // VA_EARLY: globaltimer when the V producer requested tile 0
     int vote[2][kSoftWarps];
     unsigned long long t_first;      // globaltimer when tile 0 was requested
     float red[4][kMaxM];
@@ -312,6 +324,11 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
     }
     if (warp == 1) ptx::tmem_alloc(ptx::smem_u32(&ms.tmem_base), kTmemCols);
     if (tid == 32) VA_TRACE_AT(241);
+#if VA_EARLY
+    ptx::tc_fence_before();
+    __syncthreads();   // barriers initialised, TMEM allocated: no block barrier is needed after the dependency
+    ptx::tc_fence_after();
+#endif
 
     // Programmatic dependent launch: every global access of this kernel comes after griddep_wait (the
     // prefetches above only pick lines for L2).
@@ -416,7 +433,12 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
         if (lane == 0) ms.plan = P;
         if (P.status && split == 0 && group == 0 && lane == 0 && a.dev_status) atomicOr(a.dev_status, P.status);
     }
+#if VA_EARLY
+    if (warp == 0) ptx::named_bar_arrive(2, kThreads);   // the plan and positions are published
+    else ptx::named_bar_sync(2, kThreads);
+#else
     __syncthreads();
+#endif
     if (warp != 0) P = ms.plan;
     if (!is_tree) {
 #pragma unroll
@@ -506,10 +528,40 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
     const int v_first = defer0 ? 0 : VA_STAGGER_NS ? min(1, ntiles) : min(kNV, ntiles);
     auto stagger = [&](int j) {
         if (VA_STAGGER_NS == 0) return;
-        const unsigned long long due = ms.t_first + (unsigned long long)j * VA_STAGGER_NS;
+        const unsigned long long due =
+            (VA_EARLY && warp == 2 ? ms.t_first_v : ms.t_first) + (unsigned long long)j * VA_STAGGER_NS;
         for (int spin = 0; spin < 1000000 && ptx::globaltimer_ns() < due; ++spin) __nanosleep(64);
     };
 
+    // row u of this group: the positions it sees inside this split, [lo, hi), and its mask of the node
+    // region [tree_base, hi); the reference of matrix row u (padding rows never weigh anything)
+    auto row_setup = [&](int u) {
+        if (u < kMaxRows) {
+            long long lo = 0, hi = 0;
+            unsigned m = 0xFFFFFFFFu;
+            if (!is_tree) {
+#pragma unroll
+                for (int r = 0; r < kMaxRows; ++r) {
+                    if (r == u && r < n_live_g) {
+                        const long long p = row_pos[r];
+                        lo = max(a.window > 0 ? max(0LL, p - a.window + 1) : 0LL, own_lo);
+                        hi = min(p + 1, own_hi);
+                    }
+                }
+            } else if (u < n_live_g) {
+                m = (unsigned)ms.anc[kMaxRows * group + u];
+                const long long logical = (long long)ms.base + tree_depth((int)m);   // the node's own position
+                lo = max(a.window > 0 ? max(0LL, logical - a.window + 1) : 0LL, own_lo);
+                hi = min(P.hi, own_hi);
+            }
+            if (hi < lo) hi = lo;
+            ms.row_lo[u] = lo;
+            ms.row_hi[u] = hi;
+            ms.row_anc[u] = m;
+            if (u == 0) ms.tree_base = is_tree ? (long long)ms.base : LLONG_MAX;
+        }
+        if (u < kMaxM) ms.ref[u] = u < ML ? kRefInit : INFINITY;
+    };
     // ---------------------------------------------------------------- set-up with global memory
     if (ntiles > 0) {
         if (tid == 0) {
@@ -530,39 +582,18 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
 #endif
             if (!j0) ms.t_first = ptx::globaltimer_ns();
             for (int j = j0; j < k_first; ++j) load_k(j);
-            for (int j = j0; j < v_first; ++j) load_v(j);
+            if (!VA_EARLY)
+                for (int j = j0; j < v_first; ++j) load_v(j);
         }
-        if (tid < kMaxRows) {
-            // row tid of this group: the positions it sees inside this split, [lo, hi), and its mask of
-            // the node region [tree_base, hi)
-            long long lo = 0, hi = 0;
-            unsigned m = 0xFFFFFFFFu;
-            if (!is_tree) {
-#pragma unroll
-                for (int r = 0; r < kMaxRows; ++r) {
-                    if (r == tid && r < n_live_g) {
-                        const long long p = row_pos[r];
-                        lo = max(a.window > 0 ? max(0LL, p - a.window + 1) : 0LL, own_lo);
-                        hi = min(p + 1, own_hi);
-                    }
-                }
-            } else if (tid < n_live_g) {
-                m = (unsigned)ms.anc[kMaxRows * group + tid];
-                const long long logical = (long long)ms.base + tree_depth((int)m);   // the node's own position
-                lo = max(a.window > 0 ? max(0LL, logical - a.window + 1) : 0LL, own_lo);
-                hi = min(P.hi, own_hi);
-            }
-            if (hi < lo) hi = lo;
-            ms.row_lo[tid] = lo;
-            ms.row_hi[tid] = hi;
-            ms.row_anc[tid] = m;
-            if (tid == 0) ms.tree_base = is_tree ? (long long)ms.base : LLONG_MAX;
-        }
-        if (tid < kMaxM) ms.ref[tid] = tid < ML ? kRefInit : INFINITY;   // padding rows never weigh anything
+#if !VA_EARLY
+        row_setup(tid);
+#endif
     }
+#if !VA_EARLY
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+#endif
     const uint32_t tmem = ms.tmem_base;
     volatile int* abort_flag = &ms.abort;
     if (tid == 0) {
@@ -603,6 +634,10 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
     } else if (warp == 2) {
         // ------------------------------------------------------------ V producer
         if (lane == 0) {
+            if (VA_EARLY) {   // the V producer requests its own first stages
+                ms.t_first_v = ptx::globaltimer_ns();
+                for (int j = 0; j < v_first; ++j) load_v(j);
+            }
             if (kPrefetch > 0)
                 for (int j = v_first; j < min(kNV + kPrefetch, ntiles); ++j) prefetch_tile(&tmv, &tmv2, j);
             int issued = v_first;
@@ -722,6 +757,10 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
     } else {
         // ------------------------------------------------------------ softmax / accumulator warps
         const int sw = warp - kSoftWarp0;     // 0..7
+#if VA_EARLY
+        row_setup(sw * 32 + lane);
+        ptx::named_bar_sync(1, kSoftThreads);   // the rows' extents and references are published
+#endif
         const int q = warp & 3;               // TMEM lane quadrant this warp may access
         const int ch = sw >> 2;               // column half: matrix rows [24 ch, 24 ch + 24)
         const int n0 = ch * kCols;

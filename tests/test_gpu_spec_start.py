@@ -17,7 +17,7 @@ from gpu_cases import expected, run_step, run_step_fused
 from speculative_decode_verify_gb300 import build, synth
 
 pytestmark = pytest.mark.gpu
-VARIANTS = {"_spec": ["VA_SPEC=1"], "_specskew": ["VA_SPEC=1", "VA_SPEC_SKEW=1"]}
+VARIANTS = {"_spec": ["VA_SPEC=1", "VA_EARLY=0"], "_specskew": ["VA_SPEC=1", "VA_SPEC_SKEW=1", "VA_EARLY=0"]}
 
 
 @pytest.fixture(scope="module", params=sorted(VARIANTS))

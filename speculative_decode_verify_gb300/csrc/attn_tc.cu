@@ -177,10 +177,15 @@ __device__ __forceinline__ void prewarm_tiles(const Plan& Q, int n, int slots, c
     const long long n64 = Q.t1 - Q.t0;
     const bool odd = (n64 & 1) != 0;
     const int nt = (int)((n64 + 1) >> 1);
+    const unsigned slot_t0 = nt > 0 ? (unsigned)((Q.t0 * kTile) % slots) : 0u;   // then 32-bit offsets
+    auto wrap_slot = [&](unsigned s) {
+        while (s >= (unsigned)slots) s -= (unsigned)slots;
+        return (int)s;
+    };
     for (int j = 0; j < n && j < nt; ++j) {
-        const long long t = Q.t0 + (odd ? (j > 0 ? 2LL * j - 1 : 0LL) : 2LL * j);
+        const unsigned dt = odd ? (j > 0 ? 2u * j - 1u : 0u) : 2u * j;
         const int halves = (odd && j == 0) ? 1 : 2;
-        const int s0 = (int)((t * kTile) % slots), s1 = (int)(((t + 1) * kTile) % slots);
+        const int s0 = wrap_slot(slot_t0 + dt * kTile), s1 = wrap_slot(slot_t0 + (dt + 1u) * kTile);
         if (halves == 2 && s1 == s0 + kTile) {
             for (int h = 0; h < 2; ++h) {
                 ptx::tma_prefetch_l2_2d(k128, h * 64, s0);
@@ -461,11 +466,21 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
     const bool odd = (n64 & 1) != 0;
     auto tile_t = [&](int j) { return P.t0 + (odd ? (j > 0 ? 2LL * j - 1 : 0LL) : 2LL * j); };
     auto tile_halves = [&](int j) { return (odd && j == 0) ? 1 : 2; };
+    // Slot of the split's first 64-position tile: one 64-bit remainder per thread; a tile's slots are then
+    // 32-bit offsets from it.  A tile lies less than 2 slots + 192 positions past it (the plan rejects
+    // extents wider than the cache), so a few subtractions wrap it.  (Two 64-bit remainders per request,
+    // on the path from a freed V stage to its refill, cost 0.26 us per 192K verify call.)
+    const unsigned slot_t0 = n64 > 0 ? (unsigned)((P.t0 * kTile) % a.slots) : 0u;
+    auto wrap_slot = [&](unsigned s) {
+        while (s >= (unsigned)a.slots) s -= (unsigned)a.slots;
+        return (int)s;
+    };
     auto tile_slots = [&](int j, int& slot0, int& slot1, int& halves) {
         const long long t = tile_t(j);
         halves = tile_halves(j);
-        slot0 = (int)((t * kTile) % a.slots);
-        slot1 = (int)(((t + 1) * kTile) % a.slots);
+        const unsigned off = slot_t0 + (unsigned)(t - P.t0) * (unsigned)kTile;
+        slot0 = wrap_slot(off);
+        slot1 = wrap_slot(off + (unsigned)kTile);
     };
     // L2 prefetch of K or V of tile j (same boxes as the loads)
     auto prefetch_tile = [&](const CUtensorMap* m64, const CUtensorMap* m128, int j) {

@@ -44,6 +44,13 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int rows, int box_rows)
 
 namespace q8 {
 
+#ifndef VA_POLL_EVERY
+#define VA_POLL_EVERY 64
+#endif
+// VA_POLL_EVERY: the MMA issuer's poll loop reads the timer and the abort flag (its give-up checks) once
+// every VA_POLL_EVERY rounds that find nothing ready, which shortens a round (64 against 1: -0.01 us per
+// 192K quantised verify call).
+
 // Tiles of a split pulled into L2 before the launch dependency resolves (0: none), as in the bf16 kernel.
 // Measured on GB300 at 192K: +0.4 us per launch and +2.7 us per verify_attn_q8_step call with 2 tiles
 // (+1.5 us at 1K), so off: this kernel's start is not where its time goes.
@@ -537,6 +544,7 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
             ok = ok && ptx::mbar_wait(bar(ms.q_full), 0, abort_flag, kWaitNs);
             int qk = 0, pv = 0;
             uint64_t idle_since = 0;
+            unsigned idle_polls = 0;
             while (ok && pv < ntiles) {
                 bool progressed = false;
                 if (qk < ntiles && qk <= pv + kSBufs - 1 &&
@@ -592,7 +600,8 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
                 }
                 if (progressed) {
                     idle_since = 0;
-                } else {
+                    idle_polls = 0;
+                } else if (VA_POLL_EVERY <= 1 || ++idle_polls % VA_POLL_EVERY == 0) {
                     const uint64_t now = ptx::globaltimer_ns();
                     if (idle_since == 0) idle_since = now;
                     if (*abort_flag || now - idle_since > kWaitNs) ok = false;

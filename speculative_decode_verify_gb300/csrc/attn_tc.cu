@@ -73,6 +73,13 @@ namespace tc {
 #ifndef VA_STAGGER_NS
 #define VA_STAGGER_NS 1200
 #endif
+#ifndef VA_POLL_EVERY
+#define VA_POLL_EVERY 64
+#endif
+// VA_POLL_EVERY: the MMA issuer's poll loop reads the timer and the abort flag (its give-up checks) once
+// every VA_POLL_EVERY rounds that find nothing ready, which shortens a round (64 against 1 per 192K verify
+// call: -0.10 and -0.11 us in two A/Bs, +0.01 us in a third).
+
 // Tiles of a chain call's split pulled into L2 before the launch dependency resolves (0: none), from the
 // plan of positions read at that time (a hint only: the kernel before may still be writing them; an L2
 // prefetch of the wrong tiles costs bandwidth, never a result).  It also warms the address translations of
@@ -466,11 +473,12 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
     const bool odd = (n64 & 1) != 0;
     auto tile_t = [&](int j) { return P.t0 + (odd ? (j > 0 ? 2LL * j - 1 : 0LL) : 2LL * j); };
     auto tile_halves = [&](int j) { return (odd && j == 0) ? 1 : 2; };
-    // Slot of the split's first 64-position tile: one 64-bit remainder per thread; a tile's slots are then
+    // Slot of the split's first 64-position tile: one 64-bit remainder per producer; a tile's slots are then
     // 32-bit offsets from it.  A tile lies less than 2 slots + 192 positions past it (the plan rejects
     // extents wider than the cache), so a few subtractions wrap it.  (Two 64-bit remainders per request,
     // on the path from a freed V stage to its refill, cost 0.26 us per 192K verify call.)
-    const unsigned slot_t0 = n64 > 0 ? (unsigned)((P.t0 * kTile) % a.slots) : 0u;
+    unsigned slot_t0 = 0u;   // set by the threads that call tile_slots, before their first call
+    auto set_slot_t0 = [&]() { slot_t0 = n64 > 0 ? (unsigned)((P.t0 * kTile) % a.slots) : 0u; };
     auto wrap_slot = [&](unsigned s) {
         while (s >= (unsigned)a.slots) s -= (unsigned)a.slots;
         return (int)s;
@@ -549,25 +557,24 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
     };
 
     // row u of this group: the positions it sees inside this split, [lo, hi), and its mask of the node
-    // region [tree_base, hi); the reference of matrix row u (padding rows never weigh anything)
+    // region [tree_base, hi); the reference of matrix row u (padding rows never weigh anything).  Compact
+    // code: it runs once per launch, from a cold instruction cache, on the softmax warps' way to their first
+    // tile.
     auto row_setup = [&](int u) {
         if (u < kMaxRows) {
             long long lo = 0, hi = 0;
             unsigned m = 0xFFFFFFFFu;
-            if (!is_tree) {
-#pragma unroll
-                for (int r = 0; r < kMaxRows; ++r) {
-                    if (r == u && r < n_live_g) {
-                        const long long p = row_pos[r];
-                        lo = max(a.window > 0 ? max(0LL, p - a.window + 1) : 0LL, own_lo);
-                        hi = min(p + 1, own_hi);
-                    }
+            if (u < n_live_g) {
+                long long p;   // the row's own position
+                if (!is_tree) {
+                    p = ms.pos[u];
+                    hi = min(p + 1, own_hi);
+                } else {
+                    m = (unsigned)ms.anc[kMaxRows * group + u];
+                    p = (long long)ms.base + tree_depth((int)m);
+                    hi = min(P.hi, own_hi);
                 }
-            } else if (u < n_live_g) {
-                m = (unsigned)ms.anc[kMaxRows * group + u];
-                const long long logical = (long long)ms.base + tree_depth((int)m);   // the node's own position
-                lo = max(a.window > 0 ? max(0LL, logical - a.window + 1) : 0LL, own_lo);
-                hi = min(P.hi, own_hi);
+                lo = max(a.window > 0 ? max(0LL, p - a.window + 1) : 0LL, own_lo);
             }
             if (hi < lo) hi = lo;
             ms.row_lo[u] = lo;
@@ -581,6 +588,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
     if (ntiles > 0) {
         if (tid == 0) {
             // Q, then the first stages
+            set_slot_t0();
             ptx::mbar_arrive_expect_tx(bar(ms.q_full), kQBytes);
             const uint64_t keep = ptx::policy_evict_last();   // every CTA reads the same q
             if (VA_HINT_Q) {
@@ -649,6 +657,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
     } else if (warp == 2) {
         // ------------------------------------------------------------ V producer
         if (lane == 0) {
+            set_slot_t0();
             if (VA_EARLY) {   // the V producer requests its own first stages
                 ms.t_first_v = ptx::globaltimer_ns();
                 for (int j = 0; j < v_first; ++j) load_v(j);
@@ -715,6 +724,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
             // behind its barrier.
             int qk = 0, pv = 0;
             uint64_t idle_since = 0;
+            unsigned idle_polls = 0;
             while (ok && pv < ntiles) {
                 bool progressed = false;
                 if (qk < ntiles && qk <= pv + 1 &&
@@ -758,7 +768,9 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
                 }
                 if (progressed) {
                     idle_since = 0;
-                } else {   // bounded: give up after kWaitNs without progress, or when another role aborted
+                    idle_polls = 0;
+                } else if (VA_POLL_EVERY <= 1 || ++idle_polls % VA_POLL_EVERY == 0) {
+                    // bounded: give up after kWaitNs without progress, or when another role aborted
                     const uint64_t now = ptx::globaltimer_ns();
                     if (idle_since == 0) idle_since = now;
                     if (*abort_flag || now - idle_since > kWaitNs) ok = false;
@@ -772,6 +784,9 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
     } else {
         // ------------------------------------------------------------ softmax / accumulator warps
         const int sw = warp - kSoftWarp0;     // 0..7
+#if defined(VA_DEBUG_VISIT) || VA_L2AHEAD > 0
+        set_slot_t0();
+#endif
 #if VA_EARLY
         row_setup(sw * 32 + lane);
         ptx::named_bar_sync(1, kSoftThreads);   // the rows' extents and references are published

@@ -82,10 +82,12 @@ def parse():
                     help="A/B comparison of two library builds on one GPU, alternated in ABBA BAAB order: each "
                          "argument is a comma-separated list of NAME=VALUE compile definitions ('' = the default "
                          "build); prints one JSON line with each build's per-block times and their spread")
-    ap.add_argument("--ab-what", choices=["call", "kernel", "q8call", "q8", "tree", "sample"], default="call",
+    ap.add_argument("--ab-what", choices=["call", "kernel", "q8call", "q8", "tree", "treecall", "sample"],
+                    default="call",
                     help="A/B unit: a whole verify call (verify_attn_step, graph-replayed), the split-attention "
                          "launch alone (verify_attn_full, back to back), or the same two over the quantised cache "
-                         "(verify_attn_q8_step / verify_attn_q8), or a 16-node tree verify launch (verify_attn_tree)")
+                         "(verify_attn_q8_step / verify_attn_q8), a 16-node tree verify launch (verify_attn_tree) "
+                         "or a whole tree call (the nodes' append, verify_attn_tree and the combine, graph-replayed)")
     ap.add_argument("--ab-ctx", type=int, default=CTX, help="A/B workload context (positions)")
     ap.add_argument("--ab-window", type=int, default=0, help="A/B workload window (0 = full attention)")
     ap.add_argument("--ab-blocks", type=int, default=16, help="A/B timed blocks per build (a multiple of 4)")
@@ -1162,6 +1164,9 @@ def profiling_loop(args, L, dev, stream):
                       "gbs": nbytes / us / 1e3}))
 
 
+GRAPHED = ("call", "q8call", "treecall")   # A/B units timed as CUDA graphs of whole calls
+
+
 def ab_order(n_blocks: int):
     """Drift-cancelling order of two arms ("Qwen3.8-27B on one RTX 4090", "Checking the path that actually
     runs"): ABBA then BAAB, repeated, so a linear drift in clocks or temperature weighs both arms equally."""
@@ -1221,12 +1226,18 @@ def ab_compare(args, dist: Dist):
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     for arm in arms.values():
         arm["S"] = arm["lib"].va_auto_splits(window + 7 if window else slots, window)
-        if args.ab_what == "tree":   # two node groups share the SMs
+        if args.ab_what in ("tree", "treecall"):   # two node groups share the SMs
             arm["S"] = arm["lib"].va_auto_splits_for(window + 15 if window else slots, window, sms // 2)
-    if args.ab_what == "tree":
+    if args.ab_what in ("tree", "treecall"):
         for i, c in enumerate(caches):
             tw = synth.make_tree(f"abtree{i}", 980 + i, base=ctx - synth.TREE_NODES, n_nodes=synth.TREE_NODES)
             c["tree"], c["tq"] = tw.tree.to(dev), synth.bits(tw.q).to(dev)
+            # the nodes' own rows (already in the cache) appended again by every tree call
+            c["tkn"] = c["kb"][tw.base:tw.base + tw.n_nodes].contiguous().to(dev)
+            c["tvn"] = c["vb"][tw.base:tw.base + tw.n_nodes].contiguous().to(dev)
+            c["tpos"] = (torch.arange(tw.n_nodes, dtype=torch.int32) + tw.base).to(dev)
+        for x in calls:
+            x["tout"] = torch.empty(16, 6, 128, dtype=torch.int16, device=dev)
     S = max(arm["S"] for arm in arms.values())
     ws = torch.zeros(2 * va.va_workspace_bytes(S) // 4, dtype=torch.float32, device=dev)   # room for 16 tree rows
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -1264,12 +1275,19 @@ def ab_compare(args, dist: Dist):
             st = L.verify_attn_q8(P(c["q"].data_ptr()), 8, x["n"], P(c["kc"].data_ptr()), P(c["vc"].data_ptr()),
                                   P(c["ks"].data_ptr()), P(c["vs"].data_ptr()), slots, window, P(x["pos"].data_ptr()),
                                   ctypes.c_float(synth.SCALE), S, P(po), P(pl), None, P(status.data_ptr()), sp)
-        elif args.ab_what == "tree":
+        elif args.ab_what in ("tree", "treecall"):
             po = ws.data_ptr()
             pl = po + 4 * S * 16 * 6 * 128
-            st = L.verify_attn_tree(P(c["tq"].data_ptr()), 16, 16, P(c["k"].data_ptr()), P(c["v"].data_ptr()), slots,
-                                    window, P(c["tree"].data_ptr()), ctypes.c_float(synth.SCALE), S, P(po), P(pl),
-                                    None, P(status.data_ptr()), sp)
+            st = 0
+            if args.ab_what == "treecall":
+                st = L.kv_ring_append(P(c["tkn"].data_ptr()), P(c["tvn"].data_ptr()), 16, P(c["k"].data_ptr()),
+                                      P(c["v"].data_ptr()), slots, P(c["tpos"].data_ptr()), P(status.data_ptr()), sp)
+            st = st or L.verify_attn_tree(P(c["tq"].data_ptr()), 16, 16, P(c["k"].data_ptr()), P(c["v"].data_ptr()),
+                                          slots, window, P(c["tree"].data_ptr()), ctypes.c_float(synth.SCALE), S,
+                                          P(po), P(pl), None, P(status.data_ptr()), sp)
+            if args.ab_what == "treecall":
+                st = st or L.attn_split_combine(P(po), P(pl), S, P(c["sink"].data_ptr()), 16, 16,
+                                                P(x["tout"].data_ptr()), None, sp)
         elif args.ab_what == "call":
             st = L.verify_attn_step(P(c["q"].data_ptr()), P(x["kn"].data_ptr()), P(x["vn"].data_ptr()), 8, x["n"],
                                     P(c["k"].data_ptr()), P(c["v"].data_ptr()), slots, window, P(x["pos"].data_ptr()),
@@ -1292,7 +1310,7 @@ def ab_compare(args, dist: Dist):
             for _ in range(3):
                 for x in calls:
                     launch(arm, x)
-            if args.ab_what in ("call", "q8call"):
+            if args.ab_what in GRAPHED:
                 g = torch.cuda.CUDAGraph()
                 with torch.cuda.graph(g, stream=stream):
                     for x in calls:
@@ -1301,23 +1319,23 @@ def ab_compare(args, dist: Dist):
         stream.synchronize()
         outs = {}
         for tag, arm in arms.items():   # both builds must compute the same thing
-            if args.ab_what in ("call", "q8call"):
+            if args.ab_what in GRAPHED:
                 graphs[tag].replay()
             else:
                 for x in calls:
                     launch(arm, x)
             stream.synchronize()
             outs[tag] = torch.stack([x["out"].clone() for x in calls]) if args.ab_what in ("call", "q8call") else \
-                ws.clone()
+                torch.stack([x["tout"].clone() for x in calls]) if args.ab_what == "treecall" else ws.clone()
         same = bool(torch.equal(outs["A"], outs["B"]))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         for tag in ab_order(max(4, args.ab_blocks)):
             arm = arms[tag]
-            if args.ab_what in ("call", "q8call"):
+            if args.ab_what in GRAPHED:
                 graphs[tag].replay()            # untimed: the block starts from a warm graph
             e0.record(stream)
             for _ in range(args.ab_reps):
-                if args.ab_what in ("call", "q8call"):
+                if args.ab_what in GRAPHED:
                     graphs[tag].replay()
                 else:
                     for x in calls:
@@ -1338,7 +1356,7 @@ def ab_compare(args, dist: Dist):
                       args.ab_reps * len(calls), "order": "ABBA BAAB", "A": res["A"], "B": res["B"],
                       "b_minus_a_us_median": statistics.median(d), "b_minus_a_us_min": min(d),
                       "b_minus_a_us_max": max(d), "outputs_identical": same,
-                      "unit": "us per verify call" if args.ab_what in ("call", "q8call") else
+                      "unit": "us per verify call" if args.ab_what in GRAPHED else
                       "us per split-attention launch"}))
 
 

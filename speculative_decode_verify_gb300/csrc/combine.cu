@@ -11,11 +11,14 @@
 namespace va {
 
 // Block shapes (measured inside the verify call on GB300): up to 8 verify rows (48 matrix rows x 4 column
-// quarters = 192 CTAs), 512 threads with 5 splits per thread: 25.16 us per 192K call, against 25.43 us
-// for 256 x 8, 25.42 for 512 threads over column halves, 26.2-27.9 for 128 / 1024 threads or eighths;
-// fewer, wider CTAs keep the dependent chain (loads, warp merges, one block barrier) short.  A 16-node
-// tree has 96 matrix rows (384 CTAs), which do not all fit at once in 512-thread blocks: there 256
-// threads with 8 splits each.
+// quarters = 192 CTAs), 128 threads with 10 splits per thread (one round of loads for up to 160 splits),
+// at most two CTAs on an SM: 22.70 us per 192K call against 23.46 us for 512 threads with 5 splits each
+// (which its registers also hold to two an SM; 23.47 for 256 x 5).  Alone, back to back on the same
+// partials, the 128-thread combine takes 2.6 us against 3.8 us; inside the call, where its CTAs start on
+// the SMs that the split kernel frees first, it was slower (+0.8 us) until it was held to two CTAs an SM
+// (three: -0.4 us, two: -0.77 us; 64 threads x 20 splits, two an SM: -0.36 us).  The cap is a request
+// for shared memory that the kernel does not use.  A 16-node tree has 96 matrix rows (384 CTAs): there
+// 256 threads with 8 splits each (the small combine there: +0.61 us per 16-node tree call at 192K).
 constexpr int kQuarters = 4;                       // column quarters of a matrix row: 32 columns each
 constexpr int kChunks = kD / kQuarters / 4;        // float4 chunks per quarter: 8
 constexpr float kLog2e = 1.4426950408889634f;
@@ -35,6 +38,23 @@ constexpr float kLog2e = 1.4426950408889634f;
 #ifndef VA_COMBINE_SMALL
 #define VA_COMBINE_SMALL 80
 #endif
+// Shape of the combine for more splits (up to 8 verify rows): threads per CTA and splits per thread.
+#ifndef VA_COMBINE_BIG_THREADS
+#define VA_COMBINE_BIG_THREADS 128
+#endif
+#ifndef VA_COMBINE_BIG_BATCH
+#define VA_COMBINE_BIG_BATCH 10
+#endif
+// Dynamic shared memory requested by each of those CTAs (unused): it caps how many share an SM (80 KB: two
+// of the 228 KB).  The same for the combine of more than 8 rows (trees, 60 KB: three an SM, -0.12 us per
+// 16-node tree call at 192K; 0: no cap).
+#ifndef VA_COMBINE_BIG_SMEM
+#define VA_COMBINE_BIG_SMEM 81920
+#endif
+#ifndef VA_COMBINE_TREE_SMEM
+#define VA_COMBINE_TREE_SMEM 61440
+#endif
+
 
 template <int kCombineThreads, int kBatch, int kMinBlocks = 1>   // kBatch: splits per thread loaded together
 __global__ void __launch_bounds__(kCombineThreads, kMinBlocks) combine_kernel(const float* __restrict__ part_o,
@@ -156,10 +176,17 @@ cudaError_t launch_combine(const float* part_o, const float* part_lse, int n_spl
         return e != cudaSuccess ? e : cudaGetLastError();
     }
 #endif
-    pdl_config(&cfg, attr, dim3(n_rows * kH, kQuarters), dim3(wide ? 512 : 256), 0, stream);
+    const int smem = wide ? VA_COMBINE_BIG_SMEM : VA_COMBINE_TREE_SMEM;
+    pdl_config(&cfg, attr, dim3(n_rows * kH, kQuarters), dim3(wide ? VA_COMBINE_BIG_THREADS : 256), smem, stream);
+    if (smem > 0) {   // (the kernel's static shared memory counts toward the 48 KB default limit too)
+        const cudaError_t ea = ensure_smem_attr(wide ? (const void*)combine_kernel<VA_COMBINE_BIG_THREADS, VA_COMBINE_BIG_BATCH>
+                                                     : (const void*)combine_kernel<256, 8>, smem);
+        if (ea != cudaSuccess) return ea;
+    }
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
     const cudaError_t e =
-        wide ? cudaLaunchKernelEx(&cfg, combine_kernel<512, 5>, part_o, part_lse, n_splits, sink, n_rows, n_live, o, out_lse)
+        wide ? cudaLaunchKernelEx(&cfg, combine_kernel<VA_COMBINE_BIG_THREADS, VA_COMBINE_BIG_BATCH>, part_o, part_lse,
+                                  n_splits, sink, n_rows, n_live, o, out_lse)
              : cudaLaunchKernelEx(&cfg, combine_kernel<256, 8>, part_o, part_lse, n_splits, sink, n_rows, n_live, o, out_lse);
     return e != cudaSuccess ? e : cudaGetLastError();
 }

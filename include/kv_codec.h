@@ -56,12 +56,12 @@ VA_API va_status verify_attn_q8(const va_bf16 *q, int n_rows, int n_live, const 
                                 float *part_lse, int *splits_used, int32_t *dev_status, va_stream stream);
 
 /*
- * verify_attn_q8_step - a whole verify call over the quantised cache in one call: kv_ring_append_q8 of the
- * live rows, verify_attn_q8, then attn_split_combine, on the stream in that order (three launches, each
- * waiting for the previous one by programmatic dependent launch; capturable in a CUDA graph).  Source as
- * verify_attn_q8 and kv_ring_append_q8.  (Coding the live rows inside the split kernel, as verify_attn_step
- * does for the bf16 cache, measured no faster: the small append launch is hidden behind the split kernel's
- * start.)
+ * verify_attn_q8_step - a whole verify call over the quantised cache in one call: verify_attn_q8 in which
+ * the split that owns the live rows' positions first codes them into the cache (the same bytes as
+ * kv_ring_append_q8 writes) and loads their tile after them, then attn_split_combine, on the stream in that
+ * order (two launches, the second waiting for the first by programmatic dependent launch; capturable in a
+ * CUDA graph).  Source as verify_attn_q8 and kv_ring_append_q8.  Positions the plan rejects (negative,
+ * decreasing, beyond the cache or the ring) set their dev_status bits and code no row.
  *   q, n_rows, n_live, k_codes, v_codes, k_scale, v_scale, slots, window, pos, scale, n_splits
  *                 as verify_attn_q8 (the codes and scales are updated in place)
  *   k_new, v_new  device [n_live][128] bf16, 16-byte aligned: the live rows' new K and V

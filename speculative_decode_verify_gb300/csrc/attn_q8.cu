@@ -29,6 +29,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "codec_dev.cuh"
 #include "kv_codec.h"
 #include "tc_ptx.cuh"
 #include "va_internal.cuh"
@@ -129,6 +130,7 @@ constexpr uint64_t kWaitNs = 2000000000ull;
 struct Misc {
     uint64_t k_full[kNK], k_empty[kNK], v_full[kNV], v_empty[kNV];
     uint64_t q_tma, h_ready, q_rot, q_full, s_full[kSBufs], s_free[kSBufs], vote_bar[2], p_full[2], pv_done[2], o_ready, drain;
+    uint64_t app_done;                // verify_attn_q8_step: this split's live rows are coded into the cache
     uint32_t tmem_base;
     int abort;
     int vote[2][kSoftWarps];
@@ -308,6 +310,7 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
         }
         ptx::mbar_init(bar(ms.o_ready), 1);
         ptx::mbar_init(bar(ms.drain), 1);
+        ptx::mbar_init(bar(ms.app_done), kSoftWarps);
         ms.abort = 0;
         ptx::mbar_init_fence();
     }
@@ -451,6 +454,14 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
         for (int hh = 0; hh < halves; ++hh)
             bulk_load(scale_dst + hh * 256u, scales + (hh ? s1 : s0), 256u, bar(full), pol);
     };
+    // verify_attn_q8_step: the live rows are coded into the cache by this launch (a.k_new set); a tile that
+    // holds a live row's position is requested only after this split's softmax warps have written them
+    // (app_done).  Positions never decrease, so the live rows are the positions [pos[0], hi).
+    const bool fused_append = a.k_new != nullptr;
+    auto tile_has_new = [&](int j) {
+        const long long t = P.t0 + 2LL * j;
+        return fused_append && (long long)row_pos[0] < (t + ((t + 1 < P.t1) ? 2 : 1)) * kTile;
+    };
     auto load_k = [&](int j) {
         load_tile(&tmk, &tmk2, kscale_g, base_s + kOffK + (uint32_t)(j % kNK) * kStage,
                   ptx::smem_u32(&ms.kscale[j % kNK][0]), ms.k_full[j % kNK], j);
@@ -508,7 +519,8 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
             int issued = 0;
             for (int j = 0; j < ntiles; ++j) {
                 uint64_t& empty = is_k ? ms.k_empty[j % kNK] : ms.v_empty[j % kNV];
-                if (!ptx::mbar_wait(bar(empty), ((j / depth) & 1) ^ 1, abort_flag, kWaitNs)) {
+                if ((tile_has_new(j) && !ptx::mbar_wait(bar(ms.app_done), 0, abort_flag, kWaitNs)) ||
+                    !ptx::mbar_wait(bar(empty), ((j / depth) & 1) ^ 1, abort_flag, kWaitNs)) {
                     fail();
                     break;
                 }
@@ -622,6 +634,30 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
         const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
         bool ok = true;
 
+        if (fused_append) {
+            // verify_attn_q8_step: softmax warp r codes live row r (key and value, the separate append's
+            // encoder) if its position lies in this split's tiles; a row whose successor has the same
+            // position is skipped, so the rows land as if written in row order.  The TMA loads of these
+            // rows come after the proxy fence and the barrier.
+            int pr = 0, pn = -1;
+#pragma unroll
+            for (int r = 0; r < kMaxRows; ++r) {
+                if (r == sw) pr = row_pos[r];
+                if (r == sw + 1 && r < a.n_live) pn = row_pos[r];
+            }
+            if (sw < a.n_live && pr >= P.t0 * kTile && pr < P.t1 * kTile && pn != pr) {
+                const int slot = pr % a.slots;
+                const uint2 kraw = __ldcg(reinterpret_cast<const uint2*>(a.k_new) + sw * 32 + lane);
+                const uint2 vraw = __ldcg(reinterpret_cast<const uint2*>(a.v_new) + sw * 32 + lane);
+                codec::code_key_row(kraw, lane, reinterpret_cast<uint8_t*>(const_cast<uint16_t*>(a.k)) + (size_t)slot * kD,
+                                    const_cast<float*>(kscale_g) + slot);
+                codec::code_value_row(vraw, lane, reinterpret_cast<int8_t*>(const_cast<uint16_t*>(a.v)) + (size_t)slot * kD,
+                                      const_cast<float*>(vscale_g) + slot);
+                ptx::fence_proxy_async_global();
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(ms.app_done));
+        }
         if (is_tree && warp == kSoftWarp0 && lane <= a.n_live) {   // the tree, for the row set-up
             if (lane == 0) ms.base = tree_word;
             else ms.anc[lane - 1] = tree_word;

@@ -6,9 +6,16 @@
 #include <cmath>
 #include <cstdint>
 
+#include "codec_dev.cuh"
 #include "kv_codec.h"
 #include "tc_ptx.cuh"
 #include "va_internal.cuh"
+
+// VA_Q8_FUSED_APPEND: verify_attn_q8_step codes its live rows inside the attention launch (the split
+// that owns them, before it loads their tile) instead of in a separate append launch before it.
+#ifndef VA_Q8_FUSED_APPEND
+#define VA_Q8_FUSED_APPEND 1
+#endif
 
 namespace va {
 
@@ -16,22 +23,6 @@ cudaError_t launch_attn_q8(const AttnArgs& a, const float* k_scale, const float*
 int device_sm_count();   // abi.cu: multiprocessors of the current device (0 if the query fails)
 
 namespace codec {
-
-// Two floats to E4M3 codes (round to nearest even, saturating); a zero result is coded +0.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-    uint16_t d;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
-    uint32_t b = d;
-    if ((b & 0x007Fu) == 0) b &= 0xFF00u;
-    if ((b & 0x7F00u) == 0) b &= 0x00FFu;
-    return b;
-}
-
-__device__ __forceinline__ float warp_max(float m) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    return m;
-}
 
 // One CTA per live row: warp 0 codes its key, warp 1 its value.  Lane l holds elements 4 l .. 4 l + 3.
 __global__ void __launch_bounds__(64) append_q8_kernel(const uint2* __restrict__ k_new, const uint2* __restrict__ v_new,
@@ -54,45 +45,8 @@ __global__ void __launch_bounds__(64) append_q8_kernel(const uint2* __restrict__
         const int pn = __ldcg(pos + r + 1);
         if (pn >= 0 && (size_t)(pn % slots) == slot) return;
     }
-    float x[4] = {__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u), __uint_as_float(raw.y << 16),
-                  __uint_as_float(raw.y & 0xFFFF0000u)};
-    if (warp == 0) {
-        // k' = H k: butterfly stages of width 1 and 2 inside the lane, then 4 .. 64 across lanes
-        const float t0 = __fadd_rn(x[0], x[1]), t1 = __fsub_rn(x[0], x[1]);
-        const float t2 = __fadd_rn(x[2], x[3]), t3 = __fsub_rn(x[2], x[3]);
-        x[0] = __fadd_rn(t0, t2);
-        x[1] = __fadd_rn(t1, t3);
-        x[2] = __fsub_rn(t0, t2);
-        x[3] = __fsub_rn(t1, t3);
-#pragma unroll
-        for (int m = 1; m < 32; m <<= 1) {
-            const bool upper = (lane & m) != 0;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float o = __shfl_xor_sync(0xffffffffu, x[i], m);
-                x[i] = upper ? __fsub_rn(o, x[i]) : __fadd_rn(x[i], o);
-            }
-        }
-        const float mx = warp_max(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
-        const float s = __fdiv_rn(mx, 448.0f);
-        float q[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) q[i] = s > 0.0f ? __fdiv_rn(x[i], s) : 0.0f;
-        const uint32_t codes = e4m3x2(q[0], q[1]) | (e4m3x2(q[2], q[3]) << 16);
-        *reinterpret_cast<uint32_t*>(k_codes + slot * kD + 4 * lane) = codes;
-        if (lane == 0) k_scale[slot] = s;
-    } else {
-        const float mx = warp_max(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
-        const float s = __fdiv_rn(mx, 127.0f);
-        uint32_t codes = 0;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int c = s > 0.0f ? max(-127, min(127, __float2int_rn(__fdiv_rn(x[i], s)))) : 0;
-            codes |= ((uint32_t)c & 0xFFu) << (8 * i);
-        }
-        *reinterpret_cast<uint32_t*>(v_codes + slot * kD + 4 * lane) = codes;
-        if (lane == 0) v_scale[slot] = s;
-    }
+    if (warp == 0) code_key_row(raw, lane, k_codes + slot * kD, k_scale + slot);
+    else code_value_row(raw, lane, v_codes + slot * kD, v_scale + slot);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -166,15 +120,21 @@ va_status verify_attn_q8_step(const va_bf16* q, const va_bf16* k_new, const va_b
     if (n_splits == 0) n_splits = va_auto_splits(window > 0 ? window + (n_live > 0 ? n_live - 1 : 0) : slots, window);
     float* part_o = workspace;
     float* part_lse = workspace + (size_t)n_splits * VA_MAX_ROWS * VA_Q_HEADS * VA_HEAD_DIM;
-    va_status st = kv_ring_append_q8(k_new, v_new, n_live, k_codes, v_codes, k_scale, v_scale, slots, pos, dev_status,
-                                     stream);
-    if (st != VA_OK) return st;
+    if (!VA_Q8_FUSED_APPEND) {
+        const va_status st = kv_ring_append_q8(k_new, v_new, n_live, k_codes, v_codes, k_scale, v_scale, slots, pos,
+                                               dev_status, stream);
+        if (st != VA_OK) return st;
+    }
     va::AttnArgs a;
     a.q = q; a.k = reinterpret_cast<const uint16_t*>(k_codes); a.v = reinterpret_cast<const uint16_t*>(v_codes);
     a.pos = pos; a.tree = nullptr;
     a.part_o = part_o; a.part_lse = part_lse; a.dev_status = dev_status;
     a.scale = scale; a.n_rows = n_rows; a.n_live = n_live; a.slots = slots; a.window = window;
     a.n_splits = n_splits; a.n_groups = 1;
+    if (VA_Q8_FUSED_APPEND && n_live > 0) {   // the live rows are coded by the attention launch itself
+        a.k_new = reinterpret_cast<const uint16_t*>(k_new);
+        a.v_new = reinterpret_cast<const uint16_t*>(v_new);
+    }
     cudaError_t e = va::launch_attn_q8(a, k_scale, v_scale, (cudaStream_t)stream);
     if (e == cudaSuccess)
         e = va::launch_combine(part_o, part_lse, n_splits, sink, n_rows, n_live, out, out_lse, (cudaStream_t)stream);

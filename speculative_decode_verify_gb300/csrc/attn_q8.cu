@@ -266,6 +266,9 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[kCols], int lane)
         }
 }
 
+// kAppend: the verify_attn_q8_step instantiation, which codes the live rows itself (a.k_new / a.v_new);
+// the instantiation without it carries none of that code.
+template <bool kAppend>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float* __restrict__ vscale_g,
                const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -457,7 +460,7 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
     // verify_attn_q8_step: the live rows are coded into the cache by this launch (a.k_new set); a tile that
     // holds a live row's position is requested only after this split's softmax warps have written them
     // (app_done).  Positions never decrease, so the live rows are the positions [pos[0], hi).
-    const bool fused_append = a.k_new != nullptr;
+    const bool fused_append = kAppend && a.k_new != nullptr;
     auto tile_has_new = [&](int j) {
         const long long t = P.t0 + 2LL * j;
         return fused_append && (long long)row_pos[0] < (t + ((t + 1 < P.t1) ? 2 : 1)) * kTile;
@@ -634,7 +637,7 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
         const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
         bool ok = true;
 
-        if (fused_append) {
+        if (kAppend && fused_append) {
             // verify_attn_q8_step: softmax warp r codes live row r (key and value, the separate append's
             // encoder) if its position lies in this split's tiles; a row whose successor has the same
             // position is skipped, so the rows land as if written in row order.  The TMA loads of these
@@ -1016,12 +1019,15 @@ cudaError_t launch_attn_q8(const AttnArgs& a, const float* k_scale, const float*
         !tc::cached_map(&tmv, codes, a.v, a.slots, 64) || !tc::cached_map(&tmk2, codes, a.k, a.slots, 128) ||
         !tc::cached_map(&tmv2, codes, a.v, a.slots, 128))
         return cudaErrorInvalidValue;
-    cudaError_t e = ensure_smem_attr((const void*)q8::attn_q8_kernel, (int)q8::kSmemBytes);
+    const bool append = a.k_new != nullptr;
+    cudaError_t e = ensure_smem_attr(append ? (const void*)q8::attn_q8_kernel<true> : (const void*)q8::attn_q8_kernel<false>,
+                                     (int)q8::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     pdl_config(&cfg, attr, dim3(a.n_splits, a.n_groups), dim3(q8::kThreads), q8::kSmemBytes, stream);
-    e = cudaLaunchKernelEx(&cfg, q8::attn_q8_kernel, a, k_scale, v_scale, tmq, tmk, tmv, tmk2, tmv2);
+    e = append ? cudaLaunchKernelEx(&cfg, q8::attn_q8_kernel<true>, a, k_scale, v_scale, tmq, tmk, tmv, tmk2, tmv2)
+               : cudaLaunchKernelEx(&cfg, q8::attn_q8_kernel<false>, a, k_scale, v_scale, tmq, tmk, tmv, tmk2, tmv2);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -11,12 +11,6 @@
 #include "tc_ptx.cuh"
 #include "va_internal.cuh"
 
-// VA_Q8_FUSED_APPEND: verify_attn_q8_step codes its live rows inside the attention launch (the split
-// that owns them, before it loads their tile) instead of in a separate append launch before it.
-#ifndef VA_Q8_FUSED_APPEND
-#define VA_Q8_FUSED_APPEND 1
-#endif
-
 namespace va {
 
 cudaError_t launch_attn_q8(const AttnArgs& a, const float* k_scale, const float* v_scale, cudaStream_t stream);

@@ -7,6 +7,12 @@
 
 #include "verify_attn.h"
 
+// VA_Q8_FUSED_APPEND: verify_attn_q8_step codes its live rows inside the attention launch (the split
+// that owns them, before it loads their tile) instead of in a separate append launch before it.
+#ifndef VA_Q8_FUSED_APPEND
+#define VA_Q8_FUSED_APPEND 1
+#endif
+
 namespace va {
 
 constexpr int kD = VA_HEAD_DIM;        // 128

@@ -73,6 +73,13 @@ namespace tc {
 #ifndef VA_STAGGER_NS
 #define VA_STAGGER_NS 1200
 #endif
+// VA_TREE_TEMPLATE: tree calls launch their own instantiation of the split kernel (0: one instantiation
+// tests a.tree at run time), so that each instantiation carries less code: a launch runs from a cold
+// instruction cache.
+#ifndef VA_TREE_TEMPLATE
+#define VA_TREE_TEMPLATE 1
+#endif
+
 #ifndef VA_POLL_EVERY
 #define VA_POLL_EVERY 64
 #endif
@@ -280,7 +287,9 @@ __device__ unsigned* g_visit = nullptr;
 
 // kAppend: the verify_attn_step instantiation, which writes the live rows itself (a.k_new / a.v_new);
 // the instantiation without it carries none of that code.
-template <bool kAppend>
+// kTree (with VA_TREE_TEMPLATE): the instantiation for tree calls (a.tree set); the chain instantiations
+// carry none of the tree code, nor the tree instantiation the chain plan.
+template <bool kAppend, bool kTree>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                const __grid_constant__ CUtensorMap tmv, const __grid_constant__ CUtensorMap tmk2,
@@ -293,7 +302,7 @@ attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmq, const 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x;
     const int group = blockIdx.y;     // rows [8 group, 8 group + 8) of the call
-    const bool is_tree = a.tree != nullptr;
+    const bool is_tree = VA_TREE_TEMPLATE ? kTree : a.tree != nullptr;
     const int M = min(kMaxM, a.n_rows * kH - kMaxM * group);             // matrix rows of this group
     const int n_live_g = max(0, min(kMaxRows, a.n_live - kMaxRows * group));   // live rows of this group
     const int ML = n_live_g * kH;     // live matrix rows of this group
@@ -1102,14 +1111,17 @@ cudaError_t launch_attn(const AttnArgs& a, cudaStream_t stream) {
         !tc::cached_map(&tmv2, enc, a.v, a.slots, 128))
         return cudaErrorInvalidValue;
     const bool append = a.k_new != nullptr;
-    cudaError_t e = ensure_smem_attr(append ? (const void*)tc::attn_tc_kernel<true> : (const void*)tc::attn_tc_kernel<false>,
-                                     (int)tc::kSmemBytes);
+    const bool tree = VA_TREE_TEMPLATE && a.tree != nullptr;
+    const void* fn = append ? (const void*)tc::attn_tc_kernel<true, false>
+                            : tree ? (const void*)tc::attn_tc_kernel<false, true> : (const void*)tc::attn_tc_kernel<false, false>;
+    cudaError_t e = ensure_smem_attr(fn, (int)tc::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     pdl_config(&cfg, attr, dim3(a.n_splits, a.n_groups), dim3(tc::kThreads), tc::kSmemBytes, stream);
-    e = append ? cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<true>, a, tmq, tmk, tmv, tmk2, tmv2)
-               : cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<false>, a, tmq, tmk, tmv, tmk2, tmv2);
+    e = append ? cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<true, false>, a, tmq, tmk, tmv, tmk2, tmv2)
+        : tree ? cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<false, true>, a, tmq, tmk, tmv, tmk2, tmv2)
+               : cudaLaunchKernelEx(&cfg, tc::attn_tc_kernel<false, false>, a, tmq, tmk, tmv, tmk2, tmv2);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -267,8 +267,9 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[kCols], int lane)
 }
 
 // kAppend: the verify_attn_q8_step instantiation, which codes the live rows itself (a.k_new / a.v_new);
-// the instantiation without it carries none of that code.
-template <bool kAppend>
+// the instantiation without it carries none of that code.  kTree: the instantiation for tree calls (a.tree
+// set), as in the bf16 kernel (VA_TREE_TEMPLATE).
+template <bool kAppend, bool kTree>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float* __restrict__ vscale_g,
                const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
@@ -280,7 +281,7 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
     Misc& ms = *reinterpret_cast<Misc*>(base + kOffMisc);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, group = blockIdx.y;
-    const bool is_tree = a.tree != nullptr;
+    const bool is_tree = VA_TREE_TEMPLATE ? kTree : a.tree != nullptr;
     // rows of this CTA: group g holds rows 8 g .. 8 g + 7 (one group for chains)
     const int n_live_g = is_tree ? min(max(a.n_live - kMaxRows * group, 0), kMaxRows) : a.n_live;
     const int M_all = a.n_rows * kH;
@@ -1020,14 +1021,17 @@ cudaError_t launch_attn_q8(const AttnArgs& a, const float* k_scale, const float*
         !tc::cached_map(&tmv2, codes, a.v, a.slots, 128))
         return cudaErrorInvalidValue;
     const bool append = a.k_new != nullptr;
-    cudaError_t e = ensure_smem_attr(append ? (const void*)q8::attn_q8_kernel<true> : (const void*)q8::attn_q8_kernel<false>,
-                                     (int)q8::kSmemBytes);
+    const bool tree = VA_TREE_TEMPLATE && a.tree != nullptr;
+    const void* fn = append ? (const void*)q8::attn_q8_kernel<true, false>
+                            : tree ? (const void*)q8::attn_q8_kernel<false, true> : (const void*)q8::attn_q8_kernel<false, false>;
+    cudaError_t e = ensure_smem_attr(fn, (int)q8::kSmemBytes);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     pdl_config(&cfg, attr, dim3(a.n_splits, a.n_groups), dim3(q8::kThreads), q8::kSmemBytes, stream);
-    e = append ? cudaLaunchKernelEx(&cfg, q8::attn_q8_kernel<true>, a, k_scale, v_scale, tmq, tmk, tmv, tmk2, tmv2)
-               : cudaLaunchKernelEx(&cfg, q8::attn_q8_kernel<false>, a, k_scale, v_scale, tmq, tmk, tmv, tmk2, tmv2);
+    e = append ? cudaLaunchKernelEx(&cfg, q8::attn_q8_kernel<true, false>, a, k_scale, v_scale, tmq, tmk, tmv, tmk2, tmv2)
+        : tree ? cudaLaunchKernelEx(&cfg, q8::attn_q8_kernel<false, true>, a, k_scale, v_scale, tmq, tmk, tmv, tmk2, tmv2)
+               : cudaLaunchKernelEx(&cfg, q8::attn_q8_kernel<false, false>, a, k_scale, v_scale, tmq, tmk, tmv, tmk2, tmv2);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

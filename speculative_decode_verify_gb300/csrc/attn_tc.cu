@@ -73,12 +73,6 @@ namespace tc {
 #ifndef VA_STAGGER_NS
 #define VA_STAGGER_NS 1200
 #endif
-// VA_TREE_TEMPLATE: tree calls launch their own instantiation of the split kernel (0: one instantiation
-// tests a.tree at run time), so that each instantiation carries less code: a launch runs from a cold
-// instruction cache.
-#ifndef VA_TREE_TEMPLATE
-#define VA_TREE_TEMPLATE 1
-#endif
 
 #ifndef VA_POLL_EVERY
 #define VA_POLL_EVERY 64

@@ -12,6 +12,12 @@
 #ifndef VA_Q8_FUSED_APPEND
 #define VA_Q8_FUSED_APPEND 1
 #endif
+// VA_TREE_TEMPLATE: tree calls launch their own instantiation of the split kernels (0: one instantiation
+// tests a.tree at run time), so that each instantiation carries less code: a launch runs from a cold
+// instruction cache.
+#ifndef VA_TREE_TEMPLATE
+#define VA_TREE_TEMPLATE 1
+#endif
 
 namespace va {
 

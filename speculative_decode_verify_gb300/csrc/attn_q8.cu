@@ -733,7 +733,7 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
             all_lo = max(all_lo, ms.row_lo[r]);
             all_hi = min(all_hi, ms.row_hi[r]);
         }
-        all_hi = min(all_hi, ms.tree_base);   // the node region of a tree is never interior
+        if (is_tree) all_hi = min(all_hi, ms.tree_base);   // the node region of a tree is never interior
         for (int j = 0; j < ntiles; ++j) {
             const long long t = P.t0 + 2LL * j;
             const int nkeys = (t + 1 < P.t1) ? 128 : 64;
@@ -794,7 +794,7 @@ attn_q8_kernel(const AttnArgs a, const float* __restrict__ kscale_g, const float
 #pragma unroll
                     for (int k = 0; k < kPartRows; ++k) {
                         const int r = kPartRows * ch + k;
-                        const bool in_mask = dk < 0 || (dk < 32 && ((ms.row_anc[r] >> (int)dk) & 1u));
+                        const bool in_mask = !is_tree || dk < 0 || (dk < 32 && ((ms.row_anc[r] >> (int)dk) & 1u));
                         rv[k] = (r < n_live_g) && kp >= ms.row_lo[r] && kp < ms.row_hi[r] && in_mask;
                     }
                 }

@@ -18,7 +18,8 @@ namespace va {
 // the SMs that the split kernel frees first, it was slower (+0.8 us) until it was held to two CTAs an SM
 // (three: -0.4 us, two: -0.77 us; 64 threads x 20 splits, two an SM: -0.36 us).  The cap is a request
 // for shared memory that the kernel does not use.  A 16-node tree has 96 matrix rows (384 CTAs): there
-// 256 threads with 8 splits each (the small combine there: +0.61 us per 16-node tree call at 192K).
+// 128 threads with 5 splits each, at most three CTAs an SM (the small, uncapped combine there: +0.61 us per
+// 16-node tree call at 192K).
 constexpr int kQuarters = 4;                       // column quarters of a matrix row: 32 columns each
 constexpr int kChunks = kD / kQuarters / 4;        // float4 chunks per quarter: 8
 constexpr float kLog2e = 1.4426950408889634f;
@@ -44,6 +45,19 @@ constexpr float kLog2e = 1.4426950408889634f;
 // quantised 1K 9.40 -> 8.88 us; at 8K (65 splits, 20 a lane) it was 0.41 us slower than the 128-thread one.
 #ifndef VA_COMBINE_WARP
 #define VA_COMBINE_WARP 1
+#endif
+// VA_COMBINE_WARP_TREE: the one-warp combine also for more than 8 rows (trees; 16-node tree call at a 2K
+// context, 17 splits: 10.10 -> 8.92 us).
+#ifndef VA_COMBINE_WARP_TREE
+#define VA_COMBINE_WARP_TREE 1
+#endif
+// Shape of the combine above 8 rows (trees) beyond the one-warp combine: threads and splits per thread (16-node
+// tree call at 192K, 76 splits: 35.36 us with 256 x 8, 35.07 with 256 x 3, 34.64 with 128 x 5).
+#ifndef VA_COMBINE_TREE_THREADS
+#define VA_COMBINE_TREE_THREADS 128
+#endif
+#ifndef VA_COMBINE_TREE_BATCH
+#define VA_COMBINE_TREE_BATCH 5
 #endif
 // Shape of the combine for more splits (up to 8 verify rows): threads per CTA and splits per thread.
 #ifndef VA_COMBINE_BIG_THREADS
@@ -256,7 +270,7 @@ cudaError_t launch_combine(const float* part_o, const float* part_lse, int n_spl
     cudaLaunchAttribute attr[1];
     const bool wide = n_rows <= kMaxRows;
 #if VA_COMBINE_WARP
-    if (wide && n_splits <= 48) {
+    if ((wide || VA_COMBINE_WARP_TREE) && n_splits <= 48) {
         // the instantiation with the fewest splits a lane that covers n_splits (unused load slots cost time:
         // 1K call 8.29 us with 12 a lane, 7.90 us with 3)
         pdl_config(&cfg, attr, dim3(n_rows * kH, kQuarters), dim3(32), 0, stream);
@@ -280,17 +294,20 @@ cudaError_t launch_combine(const float* part_o, const float* part_lse, int n_spl
     }
 #endif
     const int smem = wide ? VA_COMBINE_BIG_SMEM : VA_COMBINE_TREE_SMEM;
-    pdl_config(&cfg, attr, dim3(n_rows * kH, kQuarters), dim3(wide ? VA_COMBINE_BIG_THREADS : 256), smem, stream);
+    pdl_config(&cfg, attr, dim3(n_rows * kH, kQuarters), dim3(wide ? VA_COMBINE_BIG_THREADS : VA_COMBINE_TREE_THREADS),
+               smem, stream);
     if (smem > 0) {   // (the kernel's static shared memory counts toward the 48 KB default limit too)
         const cudaError_t ea = ensure_smem_attr(wide ? (const void*)combine_kernel<VA_COMBINE_BIG_THREADS, VA_COMBINE_BIG_BATCH>
-                                                     : (const void*)combine_kernel<256, 8>, smem);
+                                                     : (const void*)combine_kernel<VA_COMBINE_TREE_THREADS,
+                                                                                   VA_COMBINE_TREE_BATCH>, smem);
         if (ea != cudaSuccess) return ea;
     }
     __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
     const cudaError_t e =
         wide ? cudaLaunchKernelEx(&cfg, combine_kernel<VA_COMBINE_BIG_THREADS, VA_COMBINE_BIG_BATCH>, part_o, part_lse,
                                   n_splits, sink, n_rows, n_live, o, out_lse)
-             : cudaLaunchKernelEx(&cfg, combine_kernel<256, 8>, part_o, part_lse, n_splits, sink, n_rows, n_live, o, out_lse);
+             : cudaLaunchKernelEx(&cfg, combine_kernel<VA_COMBINE_TREE_THREADS, VA_COMBINE_TREE_BATCH>, part_o, part_lse,
+                                  n_splits, sink, n_rows, n_live, o, out_lse);
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -202,9 +202,14 @@ def test_device_status_for_bad_positions():
     assert torch.equal(ring2[7].cpu(), k[1].cpu()) and int((ring2 != 0).any(dim=1).sum()) == 1
 
 
-@pytest.mark.parametrize("S", [0, 1, 3, 4, 5, 152, 4096])
-def test_combine_alone_on_synthetic_partials(S):
-    n_rows, n_live = 8, 7
+# every shape of the combine: one warp a CTA with 1, 2, 3, 6, 9 or 12 splits a lane (S <= 48), 128 threads x 5
+# (49..80), 128 threads x 10 in one round (81..160) or more rounds; above 8 rows (trees) one warp a CTA up to 48
+# splits, else 128 threads x 5 in one or more rounds
+@pytest.mark.parametrize("n_rows,n_live,S", [(8, 7, 0), (8, 7, 1), (8, 7, 3), (8, 7, 4), (8, 7, 5), (8, 7, 9),
+                                             (8, 7, 20), (8, 7, 33), (8, 7, 48), (8, 7, 64), (8, 7, 152),
+                                             (8, 7, 160), (8, 7, 161), (8, 7, 4096), (16, 13, 17), (16, 13, 76),
+                                             (16, 16, 100)])
+def test_combine_alone_on_synthetic_partials(n_rows, n_live, S):
     po, pl, sink = synth.random_partials(31 + S, max(S, 1), n_rows, n_live)
     po, pl = po[:S], pl[:S]
     ref_out, ref_lse = oracle.combine(po.numpy(), pl.numpy(), sink.numpy(), n_live)

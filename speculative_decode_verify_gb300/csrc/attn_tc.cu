@@ -55,8 +55,11 @@ namespace tc {
 #endif
 // Start-up shaping: every CTA asks for its first tiles at the same moment and the DRAM serves all of
 // them interleaved, so tile 0 lands no earlier than the rest and no stage frees up for several us.
-// Requesting tile j of the first ring fill j * VA_STAGGER_NS after tile 0 lets tile 0 land first.
-// 1.2 us measured best on GB300 (0: no stagger).
+// Requesting tile j of the first ring fill j * VA_STAGGER_NS after tile 0 lets tile 0 land first
+// (0: no stagger).  Measured on GB300 per 192K verify call with the L2 pre-warm and the one-barrier start:
+// 1,600 ns +0.90 us against 1,200 ns; 800 ns -0.23 us, 600 ns -0.27 us, 400 ns -0.32 us (-0.64 us per
+// launch back to back), 200 ns -0.05 us against 400 ns; 0 +0.52 us against 400 ns.  (Before the pre-warm
+// 1,200 ns was best.)
 // Tiles pulled into L2 ahead of the rings by the softmax warps with plain loads (0: none).
 #ifndef VA_L2AHEAD
 #define VA_L2AHEAD 0
@@ -71,7 +74,7 @@ namespace tc {
 #define VA_HINT_Q 1
 #endif
 #ifndef VA_STAGGER_NS
-#define VA_STAGGER_NS 1200
+#define VA_STAGGER_NS 200
 #endif
 
 #ifndef VA_POLL_EVERY

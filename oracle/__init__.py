@@ -17,7 +17,7 @@ Sources (IQuestRT technical report):
   * section "Let correctness checks change the design": the ring bug was found with
     independent position labels and visible-position sets.
 
-Readings taken where the pages are silent (each is listed in the design notes):
+Readings taken where the pages are silent:
   * positions are 0-based; a row at position p sees keys j <= p;
   * the read extent comes from the live rows only: hi = max live position + 1;
   * a sliding window of W covers [p - W + 1, p] for a row at p;

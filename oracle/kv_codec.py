@@ -4,7 +4,7 @@ TEST INFRASTRUCTURE, NOT PRODUCT CODE (same rules as the rest of ``oracle/``).
 
 Source: "Qwen3.8-27B on one RTX 4090", section "A cheaper cache and state": cache values move to INT8;
 keys stay FP8 after a Hadamard rotation; verify attention gets faster.  Where the page leaves the codec
-open, the plainest reading is taken (each one is listed in the design notes):
+open, the plainest reading is taken:
 
   * one scale per cached position and tensor (per row of K and per row of V), fp32;
   * keys: k' = H k with H the 128 x 128 Sylvester Hadamard matrix of +-1 entries, evaluated by the fast

@@ -17,7 +17,7 @@ Sources:
   * "Qwen3.8-27B on one RTX 4090", section "More tokens per round: verify trees": a draft tree is
     verified in one pass.
 
-Readings where the pages leave a step open (each is listed in the design notes):
+Readings where the pages leave a step open:
   * top-k order: by logit descending, equal logits by lower token id;
   * temperature T scales logits before the softmax over the k candidates; top-p keeps the shortest
     prefix of that order whose probability sum reaches top_p (the crossing token included);
